@@ -1,0 +1,339 @@
+"""Pins for the CPU oracle, written as functions of an oracle instance.
+
+``test_oracle_pins.py`` runs them against the oracle (all must pass);
+``test_oracle_mutants.py`` runs them against copies of the oracle with one
+plausible mistake planted each (at least one must fail).  Nothing here calls
+the oracle's own decoders to produce an expected value: expected values come
+from the golden fixtures (published format tables), from PyTorch's
+float8_e4m3fn conversion, from numpy's float16 rounding, from closed forms and
+from an independent dense float64 expansion.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --- independent decoders (published tables / library conversions) --------
+
+def golden_e2m1() -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, "e2m1_values.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                c, v = line.split()
+                out[int(c, 16)] = float(v)
+    return out
+
+
+def golden_e4m3_points() -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, "e4m3fn_points.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                c, v = line.split()
+                out[int(c, 16)] = float(v)
+    return out
+
+
+def golden_atom_offsets() -> list:
+    out = []
+    with open(os.path.join(GOLDEN, "sf_atom_offsets.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append(tuple(int(x) for x in line.split()))
+    return out
+
+
+def torch_e4m3_table() -> np.ndarray:
+    b = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+E2M1_TABLE = None
+
+
+def e2m1_table() -> np.ndarray:
+    global E2M1_TABLE
+    if E2M1_TABLE is None:
+        g = golden_e2m1()
+        E2M1_TABLE = np.array([g[c] for c in range(16)], dtype=np.float64)
+    return E2M1_TABLE
+
+
+def dense(codes: np.ndarray, sf: np.ndarray, K: int) -> np.ndarray:
+    """Dense float64 [rows, K] expansion: low nibble of byte i is element 2i."""
+    rows = codes.shape[0]
+    lo = codes & 0x0F
+    hi = codes >> 4
+    elem = np.empty((rows, K), dtype=np.int64)
+    elem[:, 0::2] = lo
+    elem[:, 1::2] = hi
+    vals = e2m1_table()[elem]
+    scales = torch_e4m3_table()[sf.astype(np.int64)]
+    return vals * np.repeat(scales, 16, axis=1)
+
+
+def brute_force_fp16_bits(A, SFA, B, SFB, K) -> np.ndarray:
+    Ad = dense(A, SFA, K)
+    Bd = dense(B, SFB, K)
+    ref = Ad @ Bd.T
+    return ref.astype(np.float16).view(np.uint16)
+
+
+# --- random inputs -----------------------------------------------------------
+
+def rand_case(rng, M, N, K, full_scale_range=False):
+    A = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    if full_scale_range:
+        # every finite E4M3FN byte, either sign (the oracle must not care)
+        pool = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], dtype=np.uint8)
+        SFA = rng.choice(pool, size=(M, K // 16))
+        SFB = rng.choice(pool, size=(N, K // 16))
+    else:
+        def sc(rows):
+            e = rng.integers(-4, 1, size=(rows, K // 16))
+            m = rng.integers(0, 8, size=(rows, K // 16))
+            return (((e + 7) << 3) | m).astype(np.uint8)
+        SFA, SFB = sc(M), sc(N)
+    return A, SFA, B, SFB
+
+
+# --- the checks --------------------------------------------------------------
+
+def check_e2m1_table(o):
+    g = golden_e2m1()
+    for c in range(16):
+        v = o.e2m1(c)
+        assert v == g[c] and math.copysign(1, v) == math.copysign(1, g[c]), (c, v, g[c])
+
+
+def check_e4m3_all_codes(o):
+    t = torch_e4m3_table()
+    for b in range(256):
+        v = o.e4m3fn(b)
+        if math.isnan(t[b]):
+            assert math.isnan(v), b
+        else:
+            assert v == t[b], (hex(b), v, t[b])
+    for b, v in golden_e4m3_points().items():
+        got = o.e4m3fn(b)
+        assert (math.isnan(v) and math.isnan(got)) or got == v, (hex(b), got, v)
+
+
+def check_fp16_rounding(o, seed=5):
+    rng = np.random.default_rng(seed)
+    xs = list(rng.standard_normal(2000) * 10.0 ** rng.integers(-9, 6, size=2000))
+    # exact ties between neighbouring halves, both parities, normal and subnormal
+    h = rng.integers(1, 0x7BFF, size=600).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    xs += list((lo + hi) / 2)
+    xs += list(-(lo + hi) / 2)
+    xs += [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -24, 2.0 ** -25,
+           3 * 2.0 ** -26, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -25, 1.0 + 2.0 ** -11,
+           1.0 + 3 * 2.0 ** -11, 2049.0, 2051.0, float("inf"), float("-inf")]
+    for x in xs:
+        with np.errstate(over="ignore"):
+            want = int(np.array(x, dtype=np.float64).astype(np.float16).view(np.uint16))
+        got = o.fp16_rne_bits(float(x))
+        assert got == want, (x, hex(got), hex(want))
+    assert o.fp16_rne_bits(float("nan")) & 0x7C00 == 0x7C00
+
+
+def check_brute_force_tiny(o, seed=11):
+    rng = np.random.default_rng(seed)
+    for (M, N, K) in [(1, 1, 16), (3, 5, 16), (7, 2, 64), (8, 8, 256), (5, 3, 64), (2, 7, 256)]:
+        A, SFA, B, SFB = rand_case(rng, M, N, K)
+        got = o.gemm(A, SFA, B, SFB, M, N, K, threads=2)
+        want = brute_force_fp16_bits(A, SFA, B, SFB, K)
+        assert np.array_equal(got, want), (M, N, K)
+        els = o.gemm_elements(A, SFA, B, SFB, M, N, K,
+                              np.repeat(np.arange(M), N), np.tile(np.arange(N), M))
+        assert np.array_equal(els.reshape(M, N), want), (M, N, K)
+
+
+def check_brute_force_grouped(o, seed=12):
+    """A grouped call (a list of groups) against per-group brute force."""
+    rng = np.random.default_rng(seed)
+    shapes = [(4, 6, 64), (1, 3, 256), (6, 1, 16)]
+    cases = [rand_case(rng, *s) for s in shapes]
+    for (M, N, K), (A, SFA, B, SFB) in zip(shapes, cases):
+        got = o.gemm(A, SFA, B, SFB, M, N, K)
+        assert np.array_equal(got, brute_force_fp16_bits(A, SFA, B, SFB, K))
+
+
+def check_fixed_point(o, seed=13):
+    rng = np.random.default_rng(seed)
+    for (M, N, K, full) in [(6, 5, 256, True), (4, 9, 512, True), (3, 4, 2048, False),
+                            (2, 3, 7168, False)]:
+        A, SFA, B, SFB = rand_case(rng, M, N, K, full_scale_range=full)
+        _, acc = o.gemm(A, SFA, B, SFB, M, N, K, want_acc=True)
+        fx = o.gemm_fixed(A, SFA, B, SFB, M, N, K)
+        assert np.all(np.abs(fx) < 2 ** 53)
+        assert np.array_equal(acc * 2.0 ** 20, fx.astype(np.float64)), (M, N, K)
+
+
+def check_single_nonzero(o, seed=14):
+    rng = np.random.default_rng(seed)
+    e2 = e2m1_table()
+    e4 = torch_e4m3_table()
+    M, N, K = 5, 7, 256
+    for _ in range(12):
+        A = np.zeros((M, K // 2), np.uint8)
+        B = np.zeros((N, K // 2), np.uint8)
+        m0, n0, k0 = int(rng.integers(M)), int(rng.integers(N)), int(rng.integers(K))
+        ca, cb = int(rng.integers(1, 16)), int(rng.integers(1, 16))
+        if ca == 8:
+            ca = 9
+        if cb == 8:
+            cb = 10
+        A[m0, k0 // 2] = ca << 4 if k0 % 2 else ca
+        B[n0, k0 // 2] = cb << 4 if k0 % 2 else cb
+        _, SFA, _, SFB = rand_case(rng, M, N, K)
+        C = o.gemm(A, SFA, B, SFB, M, N, K).view(np.float16).astype(np.float64)
+        want = np.zeros((M, N))
+        want[m0, n0] = np.float16(e2[ca] * e4[SFA[m0, k0 // 16]] * e2[cb] * e4[SFB[n0, k0 // 16]])
+        assert np.array_equal(C, want), (m0, n0, k0, ca, cb)
+
+
+def check_all_ones_power_of_two(o):
+    """Every code 1.0 (nibble 0x2) with sa * sb = 2^k gives C = K * 2^k
+    exactly (+inf once that passes the largest finite FP16, 65504)."""
+    for K in (256, 1024):
+        M, N = 3, 4
+        A = np.full((M, K // 2), 0x22, np.uint8)
+        B = np.full((N, K // 2), 0x22, np.uint8)
+        for ka in range(-4, 1):
+            for kb in range(-4, 8):
+                SFA = np.full((M, K // 16), (ka + 7) << 3, np.uint8)   # 2^ka exactly
+                SFB = np.full((N, K // 16), (kb + 7) << 3, np.uint8)
+                C = o.gemm(A, SFA, B, SFB, M, N, K).view(np.float16).astype(np.float64)
+                want = K * 2.0 ** (ka + kb)
+                if want > 65504.0:          # past the largest finite half
+                    want = np.inf
+                assert np.all(C == want), (K, ka, kb, C[0, 0])
+
+
+def check_zero_scales(o, seed=15):
+    rng = np.random.default_rng(seed)
+    M, N, K = 4, 6, 512
+    A, SFA, B, SFB = rand_case(rng, M, N, K)
+    C = o.gemm(A, np.zeros_like(SFA), B, SFB, M, N, K)
+    assert np.all(C.view(np.float16).astype(np.float64) == 0.0)
+    C = o.gemm(A, SFA, B, np.zeros_like(SFB), M, N, K)
+    assert np.all(C.view(np.float16).astype(np.float64) == 0.0)
+
+
+def check_nibble_order(o):
+    """A nonzero only at k=0 (low nibble of byte 0), B only at k=1 (high
+    nibble): the product never meets, C = 0.  Both at k=1: C = a*b."""
+    K, M, N = 256, 1, 1
+    SF = np.full((1, K // 16), 0x38, np.uint8)       # 1.0
+    A = np.zeros((1, K // 2), np.uint8)
+    B = np.zeros((1, K // 2), np.uint8)
+    A[0, 0] = 0x02           # element 0 = 1.0
+    B[0, 0] = 0x40           # element 1 = 2.0
+    C = o.gemm(A, SF, B, SF, M, N, K).view(np.float16).astype(np.float64)
+    assert C[0, 0] == 0.0
+    A[0, 0] = 0x50           # element 1 = 3.0
+    C = o.gemm(A, SF, B, SF, M, N, K).view(np.float16).astype(np.float64)
+    assert C[0, 0] == 6.0
+
+
+def check_scale_blocks(o):
+    """Ones everywhere, SFA distinct per 16-block, SFB = 1: each block
+    contributes 16 * its own scale, so C = 16 * sum of the row's scales;
+    row m and column n see only their own scales."""
+    M, N, K = 3, 2, 512
+    A = np.full((M, K // 2), 0x22, np.uint8)
+    B = np.full((N, K // 2), 0x22, np.uint8)
+    e4 = torch_e4m3_table()
+    rng = np.random.default_rng(16)
+    SFA = rng.integers(0x20, 0x48, size=(M, K // 16)).astype(np.uint8)
+    SFB = np.full((N, K // 16), 0x38, np.uint8)
+    SFB[1, :] = 0x40                                  # column 1 doubled
+    C = o.gemm(A, SFA, B, SFB, M, N, K).view(np.float16).astype(np.float64)
+    for m in range(M):
+        s = 16.0 * e4[SFA[m]].sum()
+        assert C[m, 0] == np.float16(s), (m, C[m, 0], s)
+        assert C[m, 1] == np.float16(2 * s), (m, C[m, 1], 2 * s)
+
+
+def check_signs(o):
+    K = 256
+    SF = np.full((1, K // 16), 0x38, np.uint8)
+    A = np.zeros((1, K // 2), np.uint8)
+    B = np.zeros((2, K // 2), np.uint8)
+    A[0, 3] = 0x09           # element 6 = -0.5
+    B[0, 3] = 0x02           # element 6 = 1.0
+    B[1, 3] = 0x0C           # element 6 = -2.0
+    SFB = np.full((2, K // 16), 0x38, np.uint8)
+    C = o.gemm(A, SF, B, SFB, 1, 2, K).view(np.float16).astype(np.float64)
+    assert C[0, 0] == -0.5 and C[0, 1] == 1.0, C
+
+
+def check_row_and_column_split(o, seed=17):
+    """Row m of C depends only on row m of A (and column n only on row n of
+    B): splitting A or B and concatenating the outputs changes nothing; so
+    does permuting the groups of a grouped call."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 9, 11, 512
+    A, SFA, B, SFB = rand_case(rng, M, N, K)
+    full = o.gemm(A, SFA, B, SFB, M, N, K)
+    top = o.gemm(A[:4], SFA[:4], B, SFB, 4, N, K)
+    bot = o.gemm(A[4:], SFA[4:], B, SFB, M - 4, N, K)
+    assert np.array_equal(np.vstack([top, bot]), full)
+    left = o.gemm(A, SFA, B[:6], SFB[:6], M, 6, K)
+    right = o.gemm(A, SFA, B[6:], SFB[6:], M, N - 6, K)
+    assert np.array_equal(np.hstack([left, right]), full)
+    # a row-range call equals the corresponding rows of the full call
+    part = o.gemm(A, SFA, B, SFB, M, N, K, rows=(2, 7))
+    assert np.array_equal(part[2:7], full[2:7]) and not part[:2].any() and not part[7:].any()
+
+
+def check_transpose_symmetry(o, seed=18):
+    """Swapping the operands transposes C (the sum is symmetric in A, B)."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 5, 8, 256
+    A, SFA, B, SFB = rand_case(rng, M, N, K)
+    c1 = o.gemm(A, SFA, B, SFB, M, N, K)
+    c2 = o.gemm(B, SFB, A, SFA, N, M, K)
+    assert np.array_equal(c1, c2.T)
+
+
+def check_relayout(o, seed=19):
+    rng = np.random.default_rng(seed)
+    for rows, K in [(1, 64), (128, 256), (200, 512), (300, 1024), (256, 7168)]:
+        src = rng.integers(0, 256, size=(rows, K // 16), dtype=np.uint8)
+        t = o.sf_relayout(src, rows, K)
+        assert t.size == ((rows + 127) // 128) * (K // 64) * 512
+        assert np.array_equal(o.sf_unrelayout(t, rows, K), src)
+        # a permutation plus zero padding: byte histogram preserved
+        pad = t.size - src.size
+        hs = np.bincount(src.ravel(), minlength=256)
+        hs[0] += pad
+        assert np.array_equal(np.bincount(t, minlength=256), hs)
+    for rows, K, r, j, off in golden_atom_offsets():
+        src = np.zeros((rows, K // 16), np.uint8)
+        src[r, j] = 0x5A
+        t = o.sf_relayout(src, rows, K)
+        nz = np.flatnonzero(t)
+        assert nz.tolist() == [off], (rows, K, r, j, nz[:4], off)
+
+
+ALL_CHECKS = [
+    check_e2m1_table, check_e4m3_all_codes, check_fp16_rounding, check_brute_force_tiny,
+    check_brute_force_grouped, check_fixed_point, check_single_nonzero,
+    check_all_ones_power_of_two, check_zero_scales, check_nibble_order, check_scale_blocks,
+    check_signs, check_row_and_column_split, check_transpose_symmetry, check_relayout,
+]
