@@ -145,11 +145,13 @@ static void dequant_row(const uint8_t *row, const uint8_t *sf_row, int K,
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    const uint8_t *A, *SFA, *B, *SFB;
-    uint16_t *C;        /* [M][N] FP16 bits, may be NULL                      */
-    double *acc;        /* [M][N] float64 sums before rounding, may be NULL   */
+    const uint8_t *A, *SFA;
+    const double *Bdq;      /* [N][K] dequantised B, shared read-only        */
+    uint16_t *C;            /* [M][N] FP16 bits, may be NULL                 */
+    double *acc;            /* [M][N] float64 sums before rounding, may be NULL */
     int M, N, K;
-    int m_begin, m_end; /* row range of this worker                          */
+    const int32_t *rows;    /* output rows of this worker                    */
+    int nrows;
 } gemm_job;
 
 static void *gemm_worker(void *arg)
@@ -157,16 +159,13 @@ static void *gemm_worker(void *arg)
     gemm_job *j = (gemm_job *)arg;
     const int K = j->K;
     double *arow = (double *)malloc(sizeof(double) * (size_t)K);
-    double *brow = (double *)malloc(sizeof(double) * (size_t)K);
-    if (!arow || !brow) {
-        free(arow);
-        free(brow);
+    if (!arow)
         return (void *)1;
-    }
-    for (int m = j->m_begin; m < j->m_end; ++m) {
+    for (int i = 0; i < j->nrows; ++i) {
+        const int m = j->rows[i];
         dequant_row(j->A + (size_t)m * (K / 2), j->SFA + (size_t)m * (K / 16), K, arow);
         for (int n = 0; n < j->N; ++n) {
-            dequant_row(j->B + (size_t)n * (K / 2), j->SFB + (size_t)n * (K / 16), K, brow);
+            const double *brow = j->Bdq + (size_t)n * K;
             double sum = 0.0;
             for (int k = 0; k < K; ++k)
                 sum += arow[k] * brow[k];
@@ -178,7 +177,6 @@ static void *gemm_worker(void *arg)
         }
     }
     free(arow);
-    free(brow);
     return NULL;
 }
 
@@ -197,31 +195,71 @@ static int resolve_threads(int n_threads, int rows)
     return n_threads;
 }
 
-/* C rows [m_begin, m_end) of one group.  C and acc are full [M][N] buffers;
- * only the requested rows are written.  n_threads <= 0 uses every online
- * core.  Returns 0 on success, -1 on bad arguments or allocation failure. */
-int nvfp4_oracle_gemm(const uint8_t *A, const uint8_t *SFA,
-                      const uint8_t *B, const uint8_t *SFB,
-                      uint16_t *C, double *acc,
-                      int M, int N, int K, int m_begin, int m_end,
-                      int n_threads)
+typedef struct {
+    const uint8_t *X, *SFX;
+    double *out;
+    int K, r0, r1;
+} dequant_job;
+
+static void *dequant_worker(void *arg)
 {
-    if (M < 0 || N < 0 || K < 0 || (K % 16) != 0)
+    dequant_job *j = (dequant_job *)arg;
+    for (int r = j->r0; r < j->r1; ++r)
+        dequant_row(j->X + (size_t)r * (j->K / 2), j->SFX + (size_t)r * (j->K / 16), j->K,
+                    j->out + (size_t)r * j->K);
+    return NULL;
+}
+
+/* out[r][k] = dequantised element k of row r, rows split across T threads */
+static void dequant_rows_parallel(const uint8_t *X, const uint8_t *SFX, int rows, int K,
+                                  double *out, int T)
+{
+    dequant_job jobs[256];
+    pthread_t tids[256];
+    int started[256];
+    for (int t = 0; t < T; ++t) {
+        jobs[t] = (dequant_job){X, SFX, out, K, (int)((long)rows * t / T),
+                                (int)((long)rows * (t + 1) / T)};
+        started[t] = (t > 0) && pthread_create(&tids[t], NULL, dequant_worker, &jobs[t]) == 0;
+        if (t > 0 && !started[t])
+            dequant_worker(&jobs[t]);
+    }
+    dequant_worker(&jobs[0]);
+    for (int t = 1; t < T; ++t)
+        if (started[t])
+            pthread_join(tids[t], NULL);
+}
+
+/* The listed rows of C for one group.  C and acc are full [M][N] buffers;
+ * only the listed rows are written.  B is dequantised once (N*K doubles,
+ * rows split across threads), then each row of A is dequantised and dotted
+ * with every row of B, k in ascending order.  n_threads <= 0 uses every online core.  Returns 0 on
+ * success, -1 on bad arguments or allocation failure. */
+int nvfp4_oracle_gemm_rows(const uint8_t *A, const uint8_t *SFA,
+                           const uint8_t *B, const uint8_t *SFB,
+                           uint16_t *C, double *acc,
+                           int M, int N, int K, const int32_t *rows, int nrows,
+                           int n_threads)
+{
+    if (M < 0 || N < 0 || K < 0 || (K % 16) != 0 || nrows < 0)
         return -1;
-    if (m_begin < 0 || m_end > M || m_begin > m_end)
-        return -1;
-    int rows = m_end - m_begin;
-    if (rows == 0 || N == 0)
+    for (int i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= M)
+            return -1;
+    if (nrows == 0 || N == 0)
         return 0;
-    int T = resolve_threads(n_threads, rows);
+    double *Bdq = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
+    if (!Bdq)
+        return -1;
+    dequant_rows_parallel(B, SFB, N, K, Bdq, resolve_threads(n_threads, N));
+    int T = resolve_threads(n_threads, nrows);
     gemm_job jobs[256];
     pthread_t tids[256];
     int started[256];
     int rc = 0;
     for (int t = 0; t < T; ++t) {
-        jobs[t] = (gemm_job){A, SFA, B, SFB, C, acc, M, N, K,
-                             m_begin + (int)((long)rows * t / T),
-                             m_begin + (int)((long)rows * (t + 1) / T)};
+        int i0 = (int)((long)nrows * t / T), i1 = (int)((long)nrows * (t + 1) / T);
+        jobs[t] = (gemm_job){A, SFA, Bdq, C, acc, M, N, K, rows + i0, i1 - i0};
         started[t] = (t > 0) && pthread_create(&tids[t], NULL, gemm_worker, &jobs[t]) == 0;
         if (t > 0 && !started[t] && gemm_worker(&jobs[t]) != NULL)
             rc = -1;
@@ -236,6 +274,29 @@ int nvfp4_oracle_gemm(const uint8_t *A, const uint8_t *SFA,
                 rc = -1;
         }
     }
+    free(Bdq);
+    return rc;
+}
+
+/* C rows [m_begin, m_end) of one group (see nvfp4_oracle_gemm_rows). */
+int nvfp4_oracle_gemm(const uint8_t *A, const uint8_t *SFA,
+                      const uint8_t *B, const uint8_t *SFB,
+                      uint16_t *C, double *acc,
+                      int M, int N, int K, int m_begin, int m_end,
+                      int n_threads)
+{
+    if (m_begin < 0 || m_end > M || m_begin > m_end)
+        return -1;
+    int nrows = m_end - m_begin;
+    if (nrows == 0)
+        return 0;
+    int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)nrows);
+    if (!rows)
+        return -1;
+    for (int i = 0; i < nrows; ++i)
+        rows[i] = m_begin + i;
+    int rc = nvfp4_oracle_gemm_rows(A, SFA, B, SFB, C, acc, M, N, K, rows, nrows, n_threads);
+    free(rows);
     return rc;
 }
 

@@ -74,6 +74,10 @@ class Oracle:
         L.nvfp4_oracle_gemm.argtypes = [_u8p, _u8p, _u8p, _u8p, _u16p, _f64p,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.nvfp4_oracle_gemm_rows.restype = ctypes.c_int
+        L.nvfp4_oracle_gemm_rows.argtypes = [_u8p, _u8p, _u8p, _u8p, _u16p, _f64p,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             _i32p, ctypes.c_int, ctypes.c_int]
         L.nvfp4_oracle_gemm_elements.restype = ctypes.c_int
         L.nvfp4_oracle_gemm_elements.argtypes = [_u8p, _u8p, _u8p, _u8p,
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -118,6 +122,20 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle gemm failed ({rc})")
         return (C, acc) if want_acc else C
+
+    def gemm_rows(self, A, SFA, B, SFB, M: int, N: int, K: int, rows, threads: int = 0):
+        """FP16 bits of the listed rows of C: uint16 [len(rows), N]."""
+        A, SFA, B, SFB = _u8(A), _u8(SFA), _u8(B), _u8(SFB)
+        assert A.size == M * K // 2 and B.size == N * K // 2
+        assert SFA.size == M * K // 16 and SFB.size == N * K // 16
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        C = np.zeros((M, N), dtype=np.uint16)
+        rc = self.L.nvfp4_oracle_gemm_rows(_p(A, _u8p), _p(SFA, _u8p), _p(B, _u8p), _p(SFB, _u8p),
+                                           _p(C, _u16p), None, M, N, K, _p(rows, _i32p),
+                                           rows.shape[0], threads)
+        if rc != 0:
+            raise ValueError(f"oracle gemm_rows failed ({rc})")
+        return C[rows]
 
     def gemm_elements(self, A, SFA, B, SFB, M: int, N: int, K: int, ms, ns) -> np.ndarray:
         """FP16 bits of C[ms[i], ns[i]] for one group."""

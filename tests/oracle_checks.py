@@ -299,6 +299,9 @@ def check_row_and_column_split(o, seed=17):
     # a row-range call equals the corresponding rows of the full call
     part = o.gemm(A, SFA, B, SFB, M, N, K, rows=(2, 7))
     assert np.array_equal(part[2:7], full[2:7]) and not part[:2].any() and not part[7:].any()
+    # so does a call for a list of rows, in any order
+    pick = [8, 0, 5, 5, 3]
+    assert np.array_equal(o.gemm_rows(A, SFA, B, SFB, M, N, K, pick), full[pick])
 
 
 def check_transpose_symmetry(o, seed=18):

@@ -46,9 +46,9 @@ MUTANTS = {
     "output_transposed": (
         "size_t idx = (size_t)m * j->N + n;",
         "size_t idx = (size_t)n * j->M + m;"),
-    "b_scale_from_a": (
-        "dequant_row(j->B + (size_t)n * (K / 2), j->SFB + (size_t)n * (K / 16), K, brow);",
-        "dequant_row(j->B + (size_t)n * (K / 2), j->SFA + (size_t)(n % j->M) * (K / 16), K, brow);"),
+    "b_scales_of_row_zero": (
+        "dequant_row(j->X + (size_t)r * (j->K / 2), j->SFX + (size_t)r * (j->K / 16), j->K,",
+        "dequant_row(j->X + (size_t)r * (j->K / 2), j->SFX, j->K,"),
     "float32_accumulator": (
         "            double sum = 0.0;\n            for (int k = 0; k < K; ++k)\n                sum += arow",
         "            float sum = 0.0f;\n            for (int k = 0; k < K; ++k)\n                sum += arow"),
