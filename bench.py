@@ -1,0 +1,408 @@
+"""Benchmark of the NVFP4 grouped GEMM hot path on GB300.
+
+One step = the whole path over one grouped call: the scale-factor relayout
+of every SFA and SFB (one launch) and the grouped GEMM (one launch per 32
+groups), inputs resident in HBM.  The L2 is flushed (a 512 MiB write)
+before every step, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own
+grouped call of the same shapes (weak scaling, no collective on the data
+path; the host reduces the step time with a max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "grouped-call TFLOPS and µs/call; achieved fraction of max(FLOP, HBM) roofline"
+UNIT = "TFLOPS"
+FLUSH_BYTES = 512 << 20
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio, GB300
+
+# dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch from one ncu
+# capture, keyed by workload, valid only for the kernel source it was taken
+# on (sha256 prefix of csrc/gemm_kernel.cuh).  Filled from profiles/.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "block_scaled_nvfp4_group_gb300", "csrc", "gemm_kernel.cuh")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [l.split(", ") for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.05]
+        if not rows:
+            rows = [l.split(", ") for (_, l) in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                mx = float(r[3])
+                for n, v in zip(names, r[6:10]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def flops_of(shapes):
+    return sum(2 * M * N * K for M, N, K in shapes)
+
+
+def bytes_of(shapes):
+    return sum(M * K // 2 + N * K // 2 + M * K // 16 + N * K // 16 + M * N * 2
+               for M, N, K in shapes)
+
+
+def relayout_bytes_of(shapes):
+    """Algorithmic bytes of the relayout step: scales read + tiled written."""
+    from block_scaled_nvfp4_group_gb300 import ops
+    tot = 0
+    for M, N, K in shapes:
+        if M == 0:
+            continue
+        tot += M * K // 16 + N * K // 16 + ops.sf_tiled_bytes(M, K) + ops.sf_tiled_bytes(N, K)
+    return tot
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_config(wl) -> dict:
+    shapes = wl.shapes()
+    return {"workload": wl.name, "groups": len(shapes), "M_g": [s[0] for s in shapes],
+            "N": shapes[0][1], "K": shapes[0][2], "seed": wl.seed,
+            "l2": "flushed by a 512 MiB device write before every timed step"}
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle timing (reference arm and cpu_baseline)                          #
+# --------------------------------------------------------------------------- #
+
+def time_oracle(wl, budget_s: float):
+    """Time the oracle on an evenly spread sample of output rows of the
+    workload, sized to take about `budget_s` seconds on all host cores.
+    Returns (TFLOPS, description, cores, seconds)."""
+    from oracle import oracle
+    o = oracle.get()
+    cores = os.cpu_count() or 1
+    g0 = wl.groups[0]
+    # calibration: a few rows of group 0
+    t = time.perf_counter()
+    o.gemm_rows(g0.A, g0.SFA, g0.B, g0.SFB, g0.M, g0.N, g0.K, list(range(min(cores, g0.M))))
+    cal = time.perf_counter() - t
+    per_row_flop = 2 * g0.N * g0.K
+    rate = min(cores, g0.M) * per_row_flop / max(cal, 1e-6)
+    target = rate * budget_s
+    total = flops_of(wl.shapes())
+    frac = min(1.0, target / total)
+
+    def sample(frac):
+        t = time.perf_counter()
+        done = nrows = 0
+        for g in wl.groups:
+            r = max(1, int(round(g.M * frac)))
+            rows = np.linspace(0, g.M - 1, r).astype(np.int64)
+            o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
+            done += 2 * r * g.N * g.K
+            nrows += r
+        return done, nrows, time.perf_counter() - t
+
+    done, nrows, dt = sample(frac)
+    if dt < 0.5 * budget_s and frac < 1.0:       # fixed per-group costs dominated: grow once
+        frac = min(1.0, frac * budget_s / max(dt, 1e-3))
+        done, nrows, dt = sample(frac)
+    desc = (f"{nrows} of {sum(g.M for g in wl.groups)} output rows (all N columns) spread evenly "
+            f"over the {len(wl.groups)} groups, {done / 1e9:.1f} GFLOP, {dt:.1f} s")
+    return done / dt / 1e12, desc, cores, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from block_scaled_nvfp4_group_gb300 import workloads
+    wl = workloads.make_workload(args.workload)
+    budget = max(1.0, args.ref_budget_s / max(1, args.steps + args.warmup))
+    vals = []
+    desc = cores = None
+    for i in range(args.warmup + args.steps):
+        v, desc, cores, _ = time_oracle(wl, budget)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    shapes = wl.shapes()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": flops_of(shapes) / (value * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm                                                                     #
+# --------------------------------------------------------------------------- #
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from block_scaled_nvfp4_group_gb300 import ops, workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+
+    wl = workloads.make_workload(args.workload)
+    if rank > 0:    # every rank its own batch of the same shapes
+        wl = workloads.Workload(wl.name, wl.seed,
+                                workloads.make_groups(wl.shapes(), wl.seed + 7919 + 1000 * rank))
+    shapes = wl.shapes()
+    flops = flops_of(shapes)
+    gemm_bytes = bytes_of(shapes)
+    rl_bytes = relayout_bytes_of(shapes)
+    prob = DeviceProblem(wl.groups, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + (len([s for s in shapes if s[0] > 0]) + 31) // 32
+
+    # warm-up (also JIT/driver first-use costs)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        prob.step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+
+    # ---- timed: K whole steps, events around each step, flush in between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    ev_g = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        prob.relayout()
+        ev_g[i][0].record(stream)
+        prob.gemm()
+        ev_g[i][1].record(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    w1 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    gemm_ms = [a.elapsed_time(b) for a, b in ev_g]
+    total_ms = max_over_ranks(sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    gemm_ms_med = statistics.median(gemm_ms)
+    relayout_ms_med = statistics.median([s - g for s, g in zip(step_ms, gemm_ms)])
+
+    # ---- end to end through the public API with host buffers
+    pinned = []
+    h2d = 0
+    for t in prob.A + prob.B + prob.SFA + prob.SFB:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        pinned.append((h, t))
+        h2d += t.numel() * t.element_size()
+    outs = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in prob.C]
+    d2h = sum(c.numel() * c.element_size() for c in prob.C)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        for h, t in pinned:
+            t.copy_(h, non_blocking=True)
+        prob.step()
+        for o, c in zip(outs, prob.C):
+            o.copy_(c, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for h, t in pinned:
+            t.copy_(h, non_blocking=True)
+        prob.step()
+        for o, c in zip(outs, prob.C):
+            o.copy_(c, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / e2e_steps
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+
+    if rank != 0:
+        return
+
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    t_mem = gemm_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_flop = flops / (fp4_peak * 1e12)
+    bound = "hbm" if t_mem >= t_flop else "tensor"
+    gemm_s = gemm_ms_med * 1e-3
+    if bound == "hbm":
+        achieved = gemm_bytes / gemm_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = flops / gemm_s / 1e12
+        peak, unit = fp4_peak, "TFLOP/s"
+    traffic = None
+    rec = NCU_TRAFFIC.get(args.workload)
+    if rec and rec.get("kernel_sha") == kernel_source_hash():
+        traffic = rec["bytes"]
+
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
+        "config": workload_config(wl),
+        "us_per_call": {"step": ms_per_step * 1e3, "gemm_median": gemm_ms_med * 1e3,
+                        "relayout_median": relayout_ms_med * 1e3},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "nvfp4_group_gemm_kernel",
+                     "peak_source": peaks["source"] + (
+                         " (hbm_gbs)" if bound == "hbm" else
+                         " (bf16_tflops x 6, nominal fp4/bf16 dense ratio)"),
+                     "algorithmic_bytes_per_launch": gemm_bytes,
+                     "flops_per_launch": flops,
+                     "roofline_fraction_of_max_time": max(t_mem, t_flop) / gemm_s},
+        "relayout": {"us": relayout_ms_med * 1e3, "bytes": rl_bytes,
+                     "gbs": rl_bytes / (relayout_ms_med * 1e-3) / 1e9 if relayout_ms_med > 0 else None},
+        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        v, desc, cores, _ = time_oracle(wl, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="moe_gate_up")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

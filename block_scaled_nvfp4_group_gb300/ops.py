@@ -1,0 +1,101 @@
+"""PyTorch-facing wrappers of the C ABI (argument marshalling only).
+
+Tensors provide device memory and the current CUDA stream; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback:
+without the built library, or without a GB300, these calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_u8(t: torch.Tensor, name: str, numel: int) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.uint8, torch.int8) and t.element_size() != 1:
+        raise ValueError(f"{name} must hold bytes (uint8), got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} bytes, expected {numel}")
+
+
+def sf_tiled_bytes(rows: int, K: int) -> int:
+    return int(_abi.load().nvfp4_sf_tiled_bytes(rows, K))
+
+
+def sf_relayout(sf: torch.Tensor, rows: int, K: int, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Row-major [rows, K/16] E4M3FN scales (uint8) -> tiled layout (uint8)."""
+    lib = _abi.load()
+    _check_u8(sf, "sf", rows * K // 16)
+    nbytes = sf_tiled_bytes(rows, K)
+    if out is None:
+        out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=sf.device)
+    elif out.numel() < nbytes:
+        raise ValueError("out too small")
+    _abi.check(lib.nvfp4_sf_relayout(ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                     rows, K, _stream_handle(stream)), "nvfp4_sf_relayout")
+    return out
+
+
+def sf_relayout_group(items, stream=None) -> None:
+    """items: iterable of (src, dst, rows, K) device tensors; one launch."""
+    lib = _abi.load()
+    items = list(items)
+    arr = (_abi.SfRelayoutDesc * len(items))()
+    for i, (src, dst, rows, K) in enumerate(items):
+        _check_u8(src, "src", rows * K // 16)
+        if dst.numel() < sf_tiled_bytes(rows, K):
+            raise ValueError("dst too small")
+        arr[i] = _abi.SfRelayoutDesc(src.data_ptr(), dst.data_ptr(), rows, K)
+    _abi.check(lib.nvfp4_sf_relayout_group(arr, len(items), _stream_handle(stream)),
+               "nvfp4_sf_relayout_group")
+
+
+def make_group_descs(groups):
+    """groups: iterable of (A, B, SFA_tiled, SFB_tiled, C, M, N, K)."""
+    groups = list(groups)
+    arr = (_abi.GroupDesc * len(groups))()
+    for i, (A, B, SFA, SFB, C, M, N, K) in enumerate(groups):
+        if M > 0:
+            _check_u8(A, "A", M * K // 2)
+            _check_u8(B, "B", N * K // 2)
+            if SFA.numel() < sf_tiled_bytes(M, K) or SFB.numel() < sf_tiled_bytes(N, K):
+                raise ValueError("scale buffers too small")
+            if C.dtype != torch.float16 or C.numel() != M * N or not C.is_contiguous():
+                raise ValueError("C must be a contiguous float16 [M, N] tensor")
+        arr[i] = _abi.GroupDesc(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                                C.data_ptr(), M, N, K)
+    return arr
+
+
+def group_gemm(groups, stream=None, descs=None) -> None:
+    """C_g = A_g . B_g^T for every group (see include/nvfp4_group_gemm.h).
+    groups: iterable of (A, B, SFA_tiled, SFB_tiled, C, M, N, K) with device
+    tensors; C is overwritten.  `descs` may carry a prebuilt descriptor array
+    (make_group_descs) to skip the per-call marshalling."""
+    lib = _abi.load()
+    arr = descs if descs is not None else make_group_descs(groups)
+    _abi.check(lib.nvfp4_group_gemm(arr, len(arr), _stream_handle(stream)), "nvfp4_group_gemm")
+
+
+def last_device_error(stream=None) -> int:
+    return int(_abi.load().nvfp4_last_device_error(_stream_handle(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _abi.load().nvfp4_set_wait_timeout_ns(int(ns))
+
+
+def debug_drop_first_stage(enable: bool) -> None:
+    _abi.load().nvfp4_debug_drop_first_stage(1 if enable else 0)

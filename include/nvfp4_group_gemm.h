@@ -1,0 +1,138 @@
+/*
+ * nvfp4_group_gemm.h -- C ABI of the GB300 (sm_103a) NVFP4 grouped GEMM.
+ *
+ * The operation (kernelbot nvfp4-group-gemm, submissions 474067, 482269 and
+ * 496386; the header comment of the CUDA source of 474067 names the formats,
+ * tcgen05_mma_nvfp4 the block-16 scaling, and custom_kernel the per-group
+ * (A, B, C) lists with (M, N, K) problem sizes):
+ *
+ *   for every group g:
+ *     C_g[m][n] = fp16( sum_{k<K_g} a(m,k) * sfa(m, k/16) * b(n,k) * sfb(n, k/16) )
+ *
+ * a, b are FP4 E2M1 codes, sfa, sfb FP8 E4M3FN scale factors (one per 16
+ * consecutive K-elements), accumulation is FP32 on the tensor cores, the
+ * output is FP16 rounded to nearest even.  C is overwritten: there is no C
+ * input, alpha, beta or per-tensor global scale (the first MMA of every tile
+ * runs with the accumulator disabled: 474067, group_gemm_persistent_kernel,
+ * MMA warp).
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers on the current CUDA device, owned
+ *    by the caller; descriptor arrays are HOST memory, read completely before
+ *    the call returns.  Nothing is allocated per call.
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *    stream).  Return codes report argument validation and launch errors
+ *    only; a timeout inside a kernel is reported later through
+ *    nvfp4_last_device_error().
+ *  - Validation happens before any launch: an invalid argument launches
+ *    nothing.
+ *  - Thread safety: calls from several host threads are safe; calls that
+ *    overlap on the GPU must not share output buffers.
+ */
+#ifndef NVFP4_GROUP_GEMM_H
+#define NVFP4_GROUP_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define NVFP4_OK                    0
+#define NVFP4_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad size, K % 256 != 0, N % 8 != 0 ... */
+#define NVFP4_ERR_MISALIGNED       (-2) /* a pointer is not 16-byte aligned                       */
+#define NVFP4_ERR_UNSUPPORTED      (-3) /* current device is not compute capability 10.3        */
+#define NVFP4_ERR_CUDA             (-4) /* a CUDA runtime / driver call failed                   */
+#define NVFP4_ERR_TIMEOUT          (-5) /* a bounded wait inside a kernel expired                */
+#define NVFP4_ERR_TOO_MANY         (-6) /* a size exceeds a documented limit                     */
+
+/* One GEMM problem of a grouped call.
+ *  A    [M][K/2] bytes: E2M1 codes, K-major, two per byte, element 2i in the
+ *       low nibble of byte i.  16-byte aligned.
+ *  B    [N][K/2] bytes, same encoding.  16-byte aligned.
+ *  SFA  M-side scales in the TILED layout written by nvfp4_sf_relayout
+ *       (rows = M): nvfp4_sf_tiled_bytes(M, K) bytes.  16-byte aligned.
+ *  SFB  N-side scales, tiled (rows = N): nvfp4_sf_tiled_bytes(N, K) bytes.
+ *  C    [M][N] FP16, row-major, leading dimension N.  16-byte aligned.
+ *  Sizes: M >= 0 (M == 0 makes the group a no-op), N >= 8 with N % 8 == 0,
+ *  K >= 256 with K % 256 == 0, M, N, K <= 2^20. */
+typedef struct GroupDesc {
+    const void *A;
+    const void *B;
+    const void *SFA;
+    const void *SFB;
+    void *C;
+    int M, N, K;
+} GroupDesc;
+
+/* Grouped GEMM over `num_groups` problems (1 <= num_groups <= 4096) in one
+ * persistent, warp-specialised tcgen05 kernel per chunk of up to 32 groups.
+ * Groups may differ in M, N and K.  Output tiles of all groups are
+ * flattened into one work list (kernelbot nvfp4-group-gemm 474067,
+ * launch_gpu_implementation: per-group tile counts and prefix sums; 496386,
+ * launch_group_gemm: the precomputed tile table).
+ * Returns NVFP4_OK or a negative code; nothing is launched on error. */
+int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream);
+
+/* Scale-factor relayout: plain row-major E4M3FN scales [rows][K/16] (row
+ * stride K/16 bytes) -> the tiled layout the GEMM reads.  The tiled buffer is
+ * a sequence of 512-byte atoms, one per (128-row block rb, 64-element K
+ * block kb), in the order [rb][kb] (474067, TMA producer warp: scale source
+ * base + ((off_m/128) * (K/64) + off_k/64) * 512).  Inside an atom the scale
+ * of row r (0..127 in the block) and 16-element sub-block j (0..3 in the K
+ * block) is at byte (r % 32) * 16 + (r / 32) * 4 + j: the 32 x 16-byte shape
+ * one tcgen05.cp 32x128b.warpx4 moves (474067, tcgen05_cp_nvfp4).  Rows
+ * beyond `rows` in the last block are written as zero.
+ *  src   device, rows * K/16 bytes, 16-byte aligned.
+ *  dst   device, nvfp4_sf_tiled_bytes(rows, K) bytes, 16-byte aligned, must
+ *        not overlap src.
+ *  rows >= 0 (0 is a no-op), K % 256 == 0, K <= 2^20, rows <= 2^20. */
+int nvfp4_sf_relayout(const void *src, void *dst, int rows, int K, cudaStream_t stream);
+
+/* Several relayouts in one launch (for example SFA and SFB of every group of
+ * a grouped call); each entry has the meaning and limits of
+ * nvfp4_sf_relayout.  1 <= count <= 4096. */
+typedef struct SfRelayoutDesc {
+    const void *src;
+    void *dst;
+    int rows, K;
+} SfRelayoutDesc;
+int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t stream);
+
+/* Bytes of the tiled scale buffer for a [rows][K/16] scale matrix:
+ * ceil(rows / 128) * (K / 64) * 512; 0 for invalid sizes. */
+size_t nvfp4_sf_tiled_bytes(int rows, int K);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * kernels of this library on the current device set when a bounded wait
+ * expires.  Returns NVFP4_OK, NVFP4_ERR_TIMEOUT, or NVFP4_ERR_CUDA (which
+ * includes a sticky CUDA error from an earlier launch). */
+int nvfp4_last_device_error(cudaStream_t stream);
+
+/* Upper bound, in nanoseconds, for any single wait inside the GEMM kernel
+ * (default 2e9).  A wait that expires sets the device error word, makes every
+ * role of that CTA leave its loop, drains in-flight copies and returns.
+ * Values below 1e6 are raised to 1e6. */
+void nvfp4_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook, not for production use: while enabled, the next GEMM launches
+ * have CTA 0 skip the loads of its first pipeline stage, so the waits that
+ * depend on it expire after the wait timeout and the kernel reports
+ * NVFP4_ERR_TIMEOUT through nvfp4_last_device_error() (the outputs of that
+ * call are then undefined).  No fault, trap or unbounded wait results. */
+void nvfp4_debug_drop_first_stage(int enable);
+
+/* Static description of the string for a return code (never NULL). */
+const char *nvfp4_strerror(int code);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GROUP_GEMM_H */

@@ -1,0 +1,35 @@
+"""Helpers shared by the GPU tests: device problems, oracle comparison."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+RTOL = 1e-3     # |C - C_oracle| <= RTOL * |C_oracle| + ATOL, elementwise
+ATOL = 1e-2
+
+
+def require_gb300():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cc = torch.cuda.get_device_capability(0)
+    if cc != (10, 3):
+        pytest.skip(f"needs compute capability 10.3, found {cc}")
+
+
+def compare_fp16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
+    """Elementwise |gpu - oracle| <= 1e-3 |oracle| + 1e-2, and the same
+    non-finite values where the oracle has them."""
+    g = got_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    fin = np.isfinite(r)
+    assert np.array_equal(np.isfinite(g), fin), f"{what}: non-finite pattern differs"
+    assert np.array_equal(g[~fin], r[~fin]), f"{what}: inf/nan values differ"
+    err = np.abs(g[fin] - r[fin])
+    bad = err > RTOL * np.abs(r[fin]) + ATOL
+    if bad.any():
+        idx = np.argwhere(fin)[np.flatnonzero(bad)[:5]]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
+                             f"first at {idx.tolist()}: gpu {g[tuple(idx[0])]} "
+                             f"oracle {r[tuple(idx[0])]}")

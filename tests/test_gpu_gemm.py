@@ -1,0 +1,152 @@
+"""Grouped GEMM on the GPU against the CPU oracle, element by element,
+within |C - C_oracle| <= 1e-3 |C_oracle| + 1e-2 (the FP32 tensor-core sum is
+rounded once more than the exact float64 sum; one FP16 ulp is at most 2^-10
+relative)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import compare_fp16, require_gb300
+from oracle import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gb300()
+
+
+def run_and_compare(groups, rows_per_group=None, seed=0):
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+    prob = DeviceProblem(groups)
+    for c in prob.C:                   # garbage in C: every element must be written
+        c.fill_(float("nan"))
+    prob.step()
+    torch.cuda.synchronize()
+    got = prob.outputs_fp16_bits()
+    o = oracle.get()
+    rng = np.random.default_rng(seed)
+    for i, (g, c) in enumerate(zip(groups, got)):
+        if g.M == 0:
+            continue
+        if rows_per_group is None:
+            ref = o.gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K)
+            compare_fp16(c, ref, f"group {i} ({g.M}x{g.N}x{g.K})")
+        else:
+            rows = sorted(set([0, g.M - 1, min(127, g.M - 1), min(128, g.M - 1)] +
+                              rng.integers(0, g.M, size=rows_per_group).tolist()))
+            ref = o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
+            compare_fp16(c[rows], ref, f"group {i} rows {len(rows)} ({g.M}x{g.N}x{g.K})")
+    return prob
+
+
+def test_small_single_tile():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_groups([(128, 128, 256)], seed=1))
+
+
+def test_ragged_several_tiles():
+    """Several M and N tiles per group, ragged tails in M and N, one-stage
+    and multi-stage K, an empty group in the middle."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(200, 384, 1024), (77, 256, 512), (0, 256, 256), (1, 136, 256), (300, 520, 768),
+              (129, 8, 2048)]
+    run_and_compare(workloads.make_groups(shapes, seed=2))
+
+
+def test_more_stages_than_ring_and_many_tiles():
+    """K large enough to wrap the shared-memory ring several times per tile
+    and more tiles than SMs (persistent loop, both accumulator buffers)."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(384, 2048, 4096), (256, 4096, 2560)]
+    run_and_compare(workloads.make_groups(shapes, seed=3))
+
+
+def test_more_groups_than_one_launch():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    rng = np.random.default_rng(4)
+    shapes = [(int(rng.integers(1, 200)), 8 * int(rng.integers(1, 40)), 256 * int(rng.integers(1, 4)))
+              for _ in range(40)]
+    run_and_compare(workloads.make_groups(shapes, seed=4))
+
+
+def test_full_scale_range_and_signs():
+    """Scales over every finite positive E4M3FN value, sign-carrying codes:
+    magnitudes far from 1 and overflow to inf in FP16 on both sides."""
+    from block_scaled_nvfp4_group_gb300.workloads import Group
+    rng = np.random.default_rng(6)
+    groups = []
+    for (M, N, K) in [(130, 200, 512), (64, 64, 256)]:
+        pool = np.array([b for b in range(1, 0x7F)], dtype=np.uint8)
+        groups.append(Group(M, N, K,
+                            rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8),
+                            rng.choice(pool, size=(M, K // 16)),
+                            rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8),
+                            rng.choice(pool, size=(N, K // 16))))
+    run_and_compare(groups)
+
+
+def test_output_bounds_untouched():
+    """The TMA store clips at M and N: bytes around each C stay intact."""
+    from block_scaled_nvfp4_group_gb300 import ops, workloads
+    groups = workloads.make_groups([(77, 136, 512), (5, 8, 256)], seed=7)
+    items, guards = [], []
+    for g in groups:
+        A = torch.from_numpy(g.A).cuda().reshape(-1)
+        B = torch.from_numpy(g.B).cuda().reshape(-1)
+        sa = ops.sf_relayout(torch.from_numpy(g.SFA).cuda().reshape(-1), g.M, g.K)
+        sb = ops.sf_relayout(torch.from_numpy(g.SFB).cuda().reshape(-1), g.N, g.K)
+        pad = 4096
+        buf = torch.full((pad + g.M * g.N + pad,), 1234.0, dtype=torch.float16, device="cuda")
+        C = buf[pad:pad + g.M * g.N].view(g.M, g.N)
+        items.append((A, B, sa, sb, C, g.M, g.N, g.K))
+        guards.append((buf, pad))
+    ops.group_gemm(items)
+    torch.cuda.synchronize()
+    o = oracle.get()
+    for g, (buf, pad), it in zip(groups, guards, items):
+        b = buf.cpu()
+        assert (b[:pad] == 1234.0).all() and (b[pad + g.M * g.N:] == 1234.0).all()
+        ref = o.gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K)
+        compare_fp16(it[4].view(torch.int16).cpu().numpy().view(np.uint16), ref, "guarded")
+
+
+def test_repeat_calls_identical():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+    prob = DeviceProblem(workloads.make_groups([(300, 1024, 2048)] * 3, seed=8))
+    prob.step()
+    first = [c.clone() for c in prob.C]
+    for _ in range(3):
+        prob.step()
+    torch.cuda.synchronize()
+    for a, b in zip(first, prob.C):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# --- the benchmark workloads, in the launch configuration bench.py times -----
+
+def test_workload_tiny():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_workload("tiny").groups)
+
+
+def test_workload_quantized():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_workload("quantized").groups)
+
+
+def test_workload_moe_down():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_workload("moe_down").groups)
+
+
+def test_workload_moe_gate_up():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_workload("moe_gate_up").groups)
+
+
+def test_workload_square_sampled_rows():
+    from block_scaled_nvfp4_group_gb300 import workloads
+    run_and_compare(workloads.make_workload("square").groups, rows_per_group=24, seed=9)
