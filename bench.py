@@ -385,6 +385,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile(args):
+    """Minimal launch sequence for an ncu capture: `warmup` steps (flush,
+    relayout, GEMM), then one more step; no timing, no oracle."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+    torch.cuda.set_device(0)
+    wl = workloads.make_workload(args.workload)
+    prob = DeviceProblem(wl.groups, device="cuda:0")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda:0")
+    for _ in range(args.warmup + 1):
+        flush.zero_()
+        prob.step()
+    torch.cuda.synchronize()
+    from block_scaled_nvfp4_group_gb300 import ops
+    rc = ops.last_device_error()
+    print(json.dumps({"profile": args.workload, "steps": args.warmup + 1, "device_error": rc}))
+    if rc != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,11 +415,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="few launches for ncu: W warm-up steps, then one step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile:
+        run_profile(args)
     else:
         run_ours(args)
 

@@ -32,16 +32,19 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 
 
 def compile_oracle(src: str, out: str) -> str:
-    """gcc, plain C11, -O2, pthreads."""
+    """gcc, plain C11, -O2, pthreads; no contraction of a*b+c into FMA, so
+    every product and every partial sum is rounded as written on every host
+    architecture."""
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread",
-                           "-D_DEFAULT_SOURCE", "-o", tmp, src, "-lm"])
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-pthread", "-D_DEFAULT_SOURCE", "-o", tmp, src, "-lm"])
     os.replace(tmp, out)
     return out
 
 
 def build(force: bool = False) -> str:
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+            os.path.getmtime(SOURCE), os.path.getmtime(__file__)):
         compile_oracle(SOURCE, _LIB)
     return _LIB
 
