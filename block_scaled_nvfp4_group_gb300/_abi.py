@@ -35,6 +35,8 @@ class SfRelayoutDesc(ctypes.Structure):
 # name -> (restype, argtypes); every symbol declared in the header
 SIGNATURES = {
     "nvfp4_group_gemm": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int, ctypes.c_void_p]),
+    "nvfp4_group_gemm_noalloc": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
+                                                ctypes.c_void_p]),
     "nvfp4_sf_relayout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_void_p]),
     "nvfp4_sf_relayout_group": (ctypes.c_int, [ctypes.POINTER(SfRelayoutDesc), ctypes.c_int,

@@ -77,6 +77,36 @@ typedef struct GroupDesc {
  * Returns NVFP4_OK or a negative code; nothing is launched on error. */
 int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream);
 
+/* The grouped GEMM of nvfp4_group_gemm for callers that are not allowed to
+ * allocate device memory: engines and plugins that receive every byte of
+ * device memory from an arena planned ahead and may not allocate while they
+ * run, and latency-critical loops that cannot afford the device-wide
+ * synchronisation an allocation may bring.  nvfp4_group_gemm allocates a
+ * 16-byte status word on its first call on a device; this entry point
+ * allocates nothing, ever.  (The pages have no counterpart: their launchers
+ * cudaMalloc a parameter buffer.)
+ *
+ * Arguments, layouts, limits and results are those of nvfp4_group_gemm, with
+ * one more limit: the kernel's status record (two 32-bit words per kernel
+ * launch; a call launches once per 32 non-empty groups) lives in a static
+ * 256-byte array inside the library, enough for 32 launches, so a call with
+ * more than 1024 non-empty groups returns NVFP4_ERR_TOO_MANY and launches
+ * nothing.  Every GPU that loads the library holds that array until the
+ * process exits.
+ *
+ * The first call on a device does a one-time set-up with that device current
+ * (capability check, kernel attribute, the device address of the static
+ * array); make that first call before any stream capture.  Each call clears
+ * the status words it uses, on `stream`, before its launch.  All calls share
+ * the one array: calls whose work overlaps on the GPU (different streams, or
+ * several host threads) race on it, so serialise them.  A bounded wait that
+ * expires inside this variant is recorded only in that array (the next call
+ * clears it); use nvfp4_group_gemm and nvfp4_last_device_error where timeouts
+ * must be observed.  The scales must already be in the tiled layout (run
+ * nvfp4_sf_relayout where allocation is allowed, e.g. at load time; its first
+ * call on a device allocates the library's status word). */
+int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups, cudaStream_t stream);
+
 /* Scale-factor relayout: plain row-major E4M3FN scales [rows][K/16] (row
  * stride K/16 bytes) -> the tiled layout the GEMM reads.  The tiled buffer is
  * a sequence of 512-byte atoms, one per (128-row block rb, 64-element K
