@@ -2,32 +2,41 @@
 // sm_103a (GB300).
 //
 // One CTA per SM walks a flat list of output tiles of every group
-// (tile t, t + gridDim.x, ...).  Six warps, three roles:
+// (tile t, t + gridDim.x, ...).  Eight warps, four roles:
 //   warps 0-3  epilogue: tensor memory -> registers (tcgen05.ld), FP32 ->
 //              FP16 (round to nearest even), a swizzled shared-memory tile
-//              per warp and a TMA tensor store, which writes whole 128-byte
-//              row segments and clips rows >= M and columns >= N;
-//   warp 4     producer: per 256-K stage, TMA loads of the A tile
-//              [128 x 256] and the B tile [BN x 256] (128-byte swizzle) and
-//              bulk copies of the matching tiled scale atoms into a ring of
-//              STAGES shared-memory slots (mbarrier full/empty pairs);
+//              per warp and a TMA tensor store, which writes whole row
+//              segments and clips rows >= M and columns >= N;
+//   warp 4     B producer: per stage of BK K-elements, one 3-D TMA load of
+//              the B tile [BN rows x BK/2 bytes] (128-byte swizzle, BK/256
+//              chunks of 128 bytes per row) and bulk copies of the matching
+//              tiled B scale atoms;
+//   warp 6     A producer: the same for the A tile [128 x BK/2 bytes] and
+//              its scales.  Two issuing warps and multi-chunk boxes keep the
+//              TMA issue rate (a few operations per microsecond per issuing
+//              thread on GB300) from bounding the stream;
 //   warp 5     MMA issuer (one thread): tcgen05.cp of the stage's scale
-//              atoms into tensor memory, four
+//              atoms into tensor memory, BK/64
 //              tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
-//              per stage into a double-buffered FP32 accumulator, and
-//              tcgen05.commit to free the stage / hand the accumulator on.
-// The epilogue of tile t overlaps the MMAs of tile t+1.
+//              per stage into an FP32 accumulator (two of them when BN=128),
+//              and tcgen05.commit to free the stage / hand the accumulator on;
+//   warp 7     idle.
+// The ring of STAGES shared-memory slots is guarded by mbarrier full/empty
+// pairs (full counts the two producers' arrivals plus the copied bytes).
+// With two accumulators the epilogue of tile t overlaps the MMAs of t+1;
+// with one, the producers still stream tile t+1's stages meanwhile.
 //
-// The warp split, the scale addressing and the descriptor fields follow
+// The warp roles, the scale addressing and the descriptor fields follow
 // kernelbot nvfp4-group-gemm submission 474067 (group_gemm_persistent_kernel,
-// tcgen05_mma_nvfp4, tcgen05_cp_nvfp4, the TMA producer warp); the store
-// path, the bounded waits and the tensor-memory budget are this build's own.
+// tcgen05_mma_nvfp4, tcgen05_cp_nvfp4, the TMA producer warp); the split
+// producers, the store path, the bounded waits and the tensor-memory budget
+// are this build's own.
 //
 // Every mbarrier wait is bounded: when it expires the waiting role sets the
 // device error word and a shared abort flag, all roles leave their loops, the
-// producer waits (bounded) for the copies it issued, the MMA thread waits for
-// its issued tensor-core work, the epilogue waits for its stores, and the CTA
-// frees its tensor memory and exits.
+// producers wait (bounded) for the copies they issued, the MMA thread waits
+// for its issued tensor-core work, the epilogue waits for its stores, and the
+// CTA frees its tensor memory and exits.
 #pragma once
 
 #include <cuda.h>
@@ -39,13 +48,14 @@
 namespace nvfp4 {
 
 constexpr int kBM = 128;           // MMA M, rows of A per tile
-constexpr int kBK = 256;           // K elements per pipeline stage
+constexpr int kChunkK = 256;       // K elements per 128-byte chunk of a row
 constexpr int kMmaK = 64;          // K elements per tcgen05.mma (FP4)
 constexpr int kMaxGroups = 32;     // groups per launch (param block)
-constexpr int kThreads = 192;      // 4 epilogue warps + producer + MMA
-constexpr int kProducerWarp = 4;
+constexpr int kThreads = 256;      // 4 epilogue warps, B producer, MMA, A producer, idle
+constexpr int kProducerBWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kEpiBufBytes = 32 * 128;  // one warp's 32 rows x 64 FP16 columns
+constexpr int kProducerAWarp = 6;
+constexpr int kSmemLimit = 232448; // 227 KiB per CTA
 
 // error word bits (device_err[0]); device_err[1] records who expired first
 constexpr uint32_t kErrTimeout = 1u;
@@ -54,14 +64,14 @@ constexpr uint32_t kErrDrainTimeout = 2u;
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
 
 struct GemmParams {
-    CUtensorMap tmA[kMaxGroups];  // uint8 [M][K/2], box 128 x 128 B, 128B swizzle
-    CUtensorMap tmB[kMaxGroups];  // uint8 [N][K/2], box 128 x BN
-    CUtensorMap tmC[kMaxGroups];  // fp16 [M][N], box 64 x 32, 128B swizzle
+    CUtensorMap tmA[kMaxGroups];  // uint8 {128 B, M, K/256}, box {128, 128, BK/256}, 128B swizzle
+    CUtensorMap tmB[kMaxGroups];  // uint8 {128 B, N, K/256}, box {128, BN, BK/256}
+    CUtensorMap tmC[kMaxGroups];  // fp16 [M][N], box EPI_COLS x 32, swizzle = EPI_COLS * 2 B
     const uint8_t *sfa[kMaxGroups];
     const uint8_t *sfb[kMaxGroups];
     int M[kMaxGroups];
     int N[kMaxGroups];
-    int kiters[kMaxGroups];    // K / 256
+    int kchunks[kMaxGroups];   // K / 256
     int grid_m[kMaxGroups];    // ceil(M / 128)
     int tile_end[kMaxGroups];  // inclusive prefix sum of grid_m * grid_n
     int num_groups;
@@ -69,32 +79,46 @@ struct GemmParams {
     uint32_t *err;             // device error words [2]
     unsigned long long timeout_ns;
     int b_policy;              // L2 policy of B / SFB loads: 0 normal, 1 first, 2 last
-    int debug_drop_stage;      // test hook: CTA 0 never issues its first stage
+    int pf_stages;             // L2 prefetch distance for B, in stages ahead of the ring (0 = off)
+    int debug_drop_stage;      // test hook: CTA 0's B producer never issues its first stage
 };
 
-template <int BN>
+// BN: tile width; BK: K elements per stage (256 or 512); STAGES: ring depth;
+// EPI_COLS: columns per epilogue store (32 or 64); EPI_BUFS: staging
+// buffers per epilogue warp (1 or 2)
+template <int BN_, int BK_, int STAGES_, int EPI_COLS_, int EPI_BUFS_>
 struct GemmConfig {
+    static constexpr int BN = BN_;
+    static constexpr int BK = BK_;
+    static constexpr int kStages = STAGES_;
+    static constexpr int kEpiCols = EPI_COLS_;
+    static constexpr int kEpiBufs = EPI_BUFS_;
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    static_assert(BK == 256 || BK == 512, "BK must be 256 or 512");
+    static_assert(kEpiCols == 32 || kEpiCols == 64, "epilogue chunk must be 32 or 64 columns");
+    static_assert(kEpiBufs == 1 || kEpiBufs == 2, "one or two staging buffers per warp");
+    static constexpr int kChunks = BK / kChunkK;           // 128-byte chunks per row per stage
+    static constexpr int kMmas = BK / kMmaK;               // MMAs per stage (4 or 8)
     static constexpr int kAccBufs = (BN == 128) ? 2 : 1;
-    static constexpr int kStages = (BN == 128) ? 5 : 4;
-    static constexpr int kABytes = kBM * kBK / 2;        // 16 KiB
-    static constexpr int kBBytes = BN * kBK / 2;
-    static constexpr int kSfaBytes = 4 * 512;            // 4 atoms (4 x 64 K)
-    static constexpr int kSfbBytes = (BN / 128) * 4 * 512;
+    static constexpr int kABytes = kBM * BK / 2;
+    static constexpr int kBBytes = BN * BK / 2;
+    static constexpr int kSfaBytes = kMmas * 512;          // one atom per 64 K
+    static constexpr int kSfbBytes = (BN / 128) * kMmas * 512;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KiB alignment");
+    static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;  // 32 rows of one chunk
     static constexpr int kEpiOff = kStages * kStageBytes;
-    static constexpr int kBarOff = kEpiOff + 4 * 2 * kEpiBufBytes;
+    static constexpr int kBarOff = kEpiOff + 4 * kEpiBufs * kEpiBufBytes;
     // full[S], empty[S], acc_full[2], acc_empty[2], drain
     static constexpr int kNumBars = 2 * kStages + 5;
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
-    static_assert(kSmemBytes <= 232448, "exceeds 227 KiB of shared memory");
+    static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
     // tensor memory: accumulators, then the scale columns of one stage
     static constexpr int kTmemCols = 512;
     static constexpr int kSfaCol = kAccBufs * BN;
-    static constexpr int kSfbCol = kSfaCol + 4 * (kBK / kMmaK);
-    static_assert(kSfbCol + 4 * (kBK / kMmaK) * (BN / 128) <= kTmemCols, "tensor memory budget");
+    static constexpr int kSfbCol = kSfaCol + 4 * kMmas;
+    static_assert(kSfbCol + 4 * kMmas * (BN / 128) <= kTmemCols, "tensor memory budget");
     // instruction descriptor (kind::mxf4nvf4): A and B E2M1 (format 1) at
     // bits 7 and 10, both K-major, N>>3 at bit 17, UE4M3 scales (bit 23 = 0),
     // M>>7 at bit 27, scale-factor data ids 0
@@ -187,12 +211,142 @@ __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int BN>
+// stages of a tile: ceil(K / BK); the last one covers only K % BK when K is
+// not a multiple of BK (one 256-element chunk of a 512-element stage)
+template <int BK>
+__device__ __forceinline__ int stages_of(int kchunks)
+{
+    return (kchunks * kChunkK + BK - 1) / BK;
+}
+
+// 64-element K blocks (= scale atoms per row block, = MMAs) of stage `it`
+template <int BK>
+__device__ __forceinline__ int kblocks_in_stage(int kchunks, int it)
+{
+    const int left = kchunks * (kChunkK / kMmaK) - it * (BK / kMmaK);
+    return left < BK / kMmaK ? left : BK / kMmaK;
+}
+
+// walks the (tile, k-stage) sequence of one CTA: the same order the loads
+// use, so a second cursor can run ahead of them for L2 prefetches
+template <int BK>
+struct StageCursor {
+    int t, it, g, nst;
+    TileCoord tc;
+    __device__ __forceinline__ void start(const GemmParams &p, int first_tile)
+    {
+        t = first_tile;
+        it = 0;
+        g = 0;
+        nst = 0;
+        if (t < p.total_tiles) {
+            tc = tile_coord(p, t, g);
+            nst = stages_of<BK>(p.kchunks[tc.g]);
+        }
+    }
+    __device__ __forceinline__ bool valid(const GemmParams &p) const { return t < p.total_tiles; }
+    __device__ __forceinline__ void advance(const GemmParams &p)
+    {
+        if (++it == nst) {
+            it = 0;
+            t += gridDim.x;
+            if (t < p.total_tiles) {
+                tc = tile_coord(p, t, g);
+                nst = stages_of<BK>(p.kchunks[tc.g]);
+            }
+        }
+    }
+};
+
+// One producer role: `IS_B` selects B (tile width BN, scales of BN/128 row
+// blocks) or A (128 rows, scales of one row block).  Arrives once per stage
+// on full[stage] with the bytes it will deliver.
+template <class Cfg, bool IS_B>
+__device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base, uint32_t bar0,
+                                              const WaitCtx &wctx)
+{
+    constexpr int S = Cfg::kStages;
+    constexpr int ROWS = IS_B ? Cfg::BN : kBM;
+    constexpr int RB = ROWS / 128;                          // 128-row scale blocks per tile
+    constexpr uint32_t kTileOff = IS_B ? Cfg::kABytes : 0;
+    constexpr uint32_t kSfOff = Cfg::kABytes + Cfg::kBBytes + (IS_B ? Cfg::kSfaBytes : 0);
+    constexpr uint32_t kTileBytes = ROWS * Cfg::BK / 2;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+
+    const uint64_t pol = IS_B ? (p.b_policy == 1   ? ptx::policy_evict_first()
+                                 : p.b_policy == 2 ? ptx::policy_evict_last()
+                                                   : ptx::policy_evict_normal())
+                              : ptx::policy_evict_last();
+    StageCursor<Cfg::BK> pf;
+    pf.start(p, IS_B ? (int)blockIdx.x : p.total_tiles);   // the A producer never prefetches
+    for (int i = 0; i < p.pf_stages && pf.valid(p); ++i) {  // run pf_stages ahead of the loads
+        ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks, pol);
+        pf.advance(p);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;
+    bool ok = true;
+    int g = 0;
+    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(p, t, g);
+        const int kchunks = p.kchunks[tc.g];
+        const int nst = stages_of<Cfg::BK>(kchunks);
+        const int kblk = kchunks * (kChunkK / kMmaK);      // scale atoms per row block
+        const int row0 = IS_B ? tc.bn * Cfg::BN : tc.bm * kBM;
+        const CUtensorMap *tm = IS_B ? &p.tmB[tc.g] : &p.tmA[tc.g];
+        const uint8_t *sf = (IS_B ? p.sfb[tc.g] : p.sfa[tc.g]) + (size_t)(row0 / 128) * kblk * 512;
+        for (int it = 0; it < nst; ++it) {
+            if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx, kRoleProducer)) {
+                ok = false;
+                break;
+            }
+            const bool drop = IS_B && p.debug_drop_stage && blockIdx.x == 0 &&
+                              t == (int)blockIdx.x && it == 0;
+            if (!drop) {
+                const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
+                const uint32_t st = base + stage * Cfg::kStageBytes;
+                const uint32_t fb = full_bar(stage);
+                ptx::mbar_arrive_expect_tx(fb, kTileBytes + RB * nk * 512);
+                // the box always lands whole; chunks past K read as zeros
+                ptx::tma_load_3d(st + kTileOff, tm, 0, row0, it * Cfg::kChunks, fb, pol);
+#pragma unroll
+                for (int h = 0; h < RB; ++h)
+                    ptx::bulk_load(st + kSfOff + h * Cfg::kMmas * 512,
+                                   sf + ((size_t)h * kblk + (size_t)it * Cfg::kMmas) * 512,
+                                   nk * 512, fb, pol);
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            }
+            if (pf.valid(p)) {
+                ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks,
+                                     pol);
+                pf.advance(p);
+            }
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // copies issued but never consumed (after an abort anywhere in the CTA)
+    // still land in this CTA's shared memory: wait for the last issue of
+    // every slot before the CTA can exit.  On the normal path these phases
+    // completed already (the MMA thread consumed them).
+    (void)ok;
+    for (int s = 0; s < S; ++s)
+        if (issued & (1u << s))
+            wait_drain(full_bar(s), (issued_parity >> s) & 1u, wctx);
+}
+
+template <class Cfg>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_group_gemm_kernel(const __grid_constant__ GemmParams p)
 {
-    using Cfg = GemmConfig<BN>;
+    constexpr int BN = Cfg::BN;
     constexpr int S = Cfg::kStages;
+    constexpr int EC = Cfg::kEpiCols;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -213,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(full_bar(s), 2);   // one arrival per producer
             ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -224,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
-    if (warp == kProducerWarp) {
+    if (warp == kProducerBWarp) {
         ptx::tmem_alloc(tmem_slot, Cfg::kTmemCols);
         ptx::tmem_relinquish();
         ptx::tc_fence_before();
@@ -236,65 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};
     const int total = p.total_tiles;
 
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            const uint64_t pol_a = ptx::policy_evict_last();
-            const uint64_t pol_b = p.b_policy == 1   ? ptx::policy_evict_first()
-                                   : p.b_policy == 2 ? ptx::policy_evict_last()
-                                                     : ptx::policy_evict_normal();
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued = 0, issued_parity = 0;
-            bool ok = true;
-            int g = 0;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileCoord tc = tile_coord(p, t, g);
-                const int kit = p.kiters[tc.g];
-                const int kblk = kit * 4;  // 64-element K blocks per row block
-                const CUtensorMap *tma = &p.tmA[tc.g];
-                const CUtensorMap *tmb = &p.tmB[tc.g];
-                const uint8_t *sfa = p.sfa[tc.g] + (size_t)tc.bm * kblk * 512;
-                const uint8_t *sfb = p.sfb[tc.g] + (size_t)tc.bn * (BN / 128) * kblk * 512;
-                for (int it = 0; it < kit; ++it) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx, kRoleProducer)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool drop = p.debug_drop_stage && blockIdx.x == 0 && t == (int)blockIdx.x &&
-                                      it == 0;
-                    if (!drop) {
-                        const uint32_t sa = base + stage * Cfg::kStageBytes;
-                        const uint32_t sb = sa + Cfg::kABytes;
-                        const uint32_t ssfa = sb + Cfg::kBBytes;
-                        const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
-                        const uint32_t fb = full_bar(stage);
-                        ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-                        ptx::tma_load_2d(sa, tma, it * (kBK / 2), tc.bm * kBM, fb, pol_a);
-                        ptx::tma_load_2d(sb, tmb, it * (kBK / 2), tc.bn * BN, fb, pol_b);
-                        ptx::bulk_load(ssfa, sfa + (size_t)it * 4 * 512, Cfg::kSfaBytes, fb, pol_a);
-#pragma unroll
-                        for (int h = 0; h < BN / 128; ++h)
-                            ptx::bulk_load(ssfb + h * 2048, sfb + ((size_t)h * kblk + it * 4) * 512,
-                                           2048, fb, pol_b);
-                        issued |= 1u << stage;
-                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    }
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // copies issued but never consumed (after an abort anywhere in
-            // the CTA) still land in this CTA's shared memory: wait for the
-            // last issue of every slot before the CTA can exit (immediate on
-            // the normal path, where the MMA thread consumed them all)
-            (void)ok;
-            for (int s = 0; s < S; ++s)
-                if (issued & (1u << s))
-                    wait_drain(full_bar(s), (issued_parity >> s) & 1u, wctx);
-        }
+    if (warp == kProducerBWarp) {
+        if (lane == 0)
+            producer_role<Cfg, true>(p, base, bar0, wctx);
+    } else if (warp == kProducerAWarp) {
+        if (lane == 0)
+            producer_role<Cfg, false>(p, base, bar0, wctx);
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
@@ -306,40 +407,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileCoord tc = tile_coord(p, t, g);
-                const int kit = p.kiters[tc.g];
+                const int kchunks = p.kchunks[tc.g];
+                const int nst = stages_of<Cfg::BK>(kchunks);
                 if (!wait_bounded(acce_bar(acc), acc_phase ^ 1u, wctx, kRoleMma)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int it = 0; it < kit; ++it) {
+                for (int it = 0; it < nst; ++it) {
                     if (!wait_bounded(full_bar(stage), phase, wctx, kRoleMma)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
                     const uint32_t sa = base + stage * Cfg::kStageBytes;
                     const uint32_t sb = sa + Cfg::kABytes;
                     const uint32_t ssfa = sb + Cfg::kBBytes;
                     const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
 #pragma unroll
-                    for (int j = 0; j < kBK / kMmaK; ++j) {
-                        ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::kSfaCol + 4 * j,
-                                                  desc_scale_atom(ssfa + 512 * j));
+                    for (int j = 0; j < Cfg::kMmas; ++j) {
+                        if (j < nk) {
+                            ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::kSfaCol + 4 * j,
+                                                      desc_scale_atom(ssfa + 512 * j));
 #pragma unroll
-                        for (int h = 0; h < BN / 128; ++h)
-                            ptx::tc_cp_32x128b_warpx4(
-                                tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j + 4 * h,
-                                desc_scale_atom(ssfb + 2048 * h + 512 * j));
+                            for (int h = 0; h < BN / 128; ++h)
+                                ptx::tc_cp_32x128b_warpx4(
+                                    tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j + 4 * h,
+                                    desc_scale_atom(ssfb + Cfg::kMmas * 512 * h + 512 * j));
+                        }
                     }
 #pragma unroll
-                    for (int j = 0; j < kBK / kMmaK; ++j) {
-                        ptx::tc_mma_nvfp4(d_tmem, desc_operand_sw128(sa + 32 * j),
-                                          desc_operand_sw128(sb + 32 * j), Cfg::kIdesc,
-                                          tmem_base + Cfg::kSfaCol + 4 * j,
-                                          tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j,
-                                          (it > 0 || j > 0) ? 1u : 0u);
+                    for (int j = 0; j < Cfg::kMmas; ++j) {
+                        if (j < nk) {
+                            // MMA j reads bytes [32 (j % 4), +32) of every row of chunk j / 4
+                            const uint32_t koff_a = (j / 4) * kBM * 128 + (j % 4) * 32;
+                            const uint32_t koff_b = (j / 4) * BN * 128 + (j % 4) * 32;
+                            ptx::tc_mma_nvfp4(d_tmem, desc_operand_sw128(sa + koff_a),
+                                              desc_operand_sw128(sb + koff_b), Cfg::kIdesc,
+                                              tmem_base + Cfg::kSfaCol + 4 * j,
+                                              tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j,
+                                              (it > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     ptx::tc_commit(empty_bar(stage));
                     issued_any = true;
@@ -363,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_drain(drain_bar, 0u, wctx);
             }
         }
-    } else {
+    } else if (warp < 4) {
         // ---------------------------------------------------- epilogue
         int acc = 0;
         uint32_t acc_phase = 0;
         int sbuf = 0;
         int g = 0;
-        const uint32_t stage_buf = base + Cfg::kEpiOff + warp * 2 * kEpiBufBytes;
+        const uint32_t stage_buf = base + Cfg::kEpiOff + warp * Cfg::kEpiBufs * Cfg::kEpiBufBytes;
         const uint32_t lane_tmem = (uint32_t)(warp * 32) << 16;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const TileCoord tc = tile_coord(p, t, g);
@@ -388,39 +498,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = tc.bn * BN;
             if (m0 < M) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
-                    if (n0 + c * 64 >= N)
+                for (int c = 0; c < BN / EC; ++c) {
+                    if (n0 + c * EC >= N)
                         break;
-                    uint32_t v0[32], v1[32];
-                    const uint32_t ta = tmem_base + lane_tmem + acc * BN + c * 64;
-                    ptx::tmem_ld_32x32b_x32(ta, v0);
-                    ptx::tmem_ld_32x32b_x32(ta + 32, v1);
-                    ptx::tmem_wait_ld();
-                    uint32_t h[32];
+                    uint32_t h[EC / 2];
+                    {
+                        const uint32_t ta = tmem_base + lane_tmem + acc * BN + c * EC;
+                        uint32_t v0[32];
+                        ptx::tmem_ld_32x32b_x32(ta, v0);
+                        if constexpr (EC == 64) {
+                            uint32_t v1[32];
+                            ptx::tmem_ld_32x32b_x32(ta + 32, v1);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        h[i] = pack_half2_rn(v0[2 * i], v0[2 * i + 1]);
-                        h[16 + i] = pack_half2_rn(v1[2 * i], v1[2 * i + 1]);
+                            for (int i = 0; i < 16; ++i) {
+                                h[i] = pack_half2_rn(v0[2 * i], v0[2 * i + 1]);
+                                h[16 + i] = pack_half2_rn(v1[2 * i], v1[2 * i + 1]);
+                            }
+                        } else {
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                h[i] = pack_half2_rn(v0[2 * i], v0[2 * i + 1]);
+                        }
                     }
-                    // the store that used this buffer two chunks ago must
-                    // have finished reading it
-                    if (lane == 0)
-                        ptx::bulk_wait_group_read<1>();
+                    // the store that last used this buffer must have finished
+                    // reading it
+                    if (lane == 0) {
+                        if constexpr (Cfg::kEpiBufs == 2)
+                            ptx::bulk_wait_group_read<1>();
+                        else
+                            ptx::bulk_wait_group_read<0>();
+                    }
                     __syncwarp();
-                    const uint32_t buf = stage_buf + sbuf * kEpiBufBytes;
-                    const uint32_t row = buf + lane * 128;
+                    const uint32_t buf = stage_buf + sbuf * Cfg::kEpiBufBytes;
+                    // one row of EC halves per lane; 16-byte chunk q of row r
+                    // sits at chunk q ^ (swizzle phase of r), the pattern of
+                    // the C tensor map's EC*2-byte swizzle (conflict-free)
+                    constexpr int kQ = EC / 8;
+                    const uint32_t row = buf + lane * (EC * 2);
+                    const int phase_r = (EC == 64) ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        ptx::st_shared_v4(row + ((q ^ (lane & 7)) << 4), h[4 * q], h[4 * q + 1],
+                    for (int q = 0; q < kQ; ++q)
+                        ptx::st_shared_v4(row + ((q ^ phase_r) << 4), h[4 * q], h[4 * q + 1],
                                           h[4 * q + 2], h[4 * q + 3]);
                     ptx::fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_2d(&p.tmC[tc.g], buf, n0 + c * 64, m0);
+                        ptx::tma_store_2d(&p.tmC[tc.g], buf, n0 + c * EC, m0);
                         ptx::bulk_commit_group();
                     }
                     __syncwarp();
-                    sbuf ^= 1;
+                    if constexpr (Cfg::kEpiBufs == 2)
+                        sbuf ^= 1;
                 }
             }
             // every lane's loads have completed (wait::ld): hand the
@@ -441,11 +571,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == kProducerWarp) {
+    if (warp == kProducerBWarp) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
 }
+
+// ---------------------------------------------------------------------------
+// Kernel configurations, chosen per call by the host (group_gemm.cu).
+//   CfgStream:  HBM-bound shapes, BN = 128 -- 512-K stages (256 contiguous
+//               bytes per row per load), 3 stages, two accumulators, one
+//               2 KiB staging buffer per epilogue warp
+//   CfgWide:    BN = 256 -- half the A re-reads, 512-K stages, 2 stages, one
+//               accumulator
+//   CfgWide4:   BN = 256 with 256-K stages, 4 stages
+//   CfgCompute: BN = 128, 256-K stages, 5 stages, two 4 KiB staging buffers
+//               per warp (64-column stores) so the epilogue keeps up
+// ---------------------------------------------------------------------------
+using CfgStream = GemmConfig<128, 512, 3, 32, 1>;
+using CfgWide = GemmConfig<256, 512, 2, 32, 1>;
+using CfgWide4 = GemmConfig<256, 256, 4, 32, 1>;
+using CfgCompute = GemmConfig<128, 256, 5, 64, 2>;
 
 }  // namespace nvfp4

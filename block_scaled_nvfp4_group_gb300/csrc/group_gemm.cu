@@ -1,5 +1,7 @@
-// group_gemm.cu -- C-ABI entry point nvfp4_group_gemm: validation, the
-// per-call tile plan, tensor maps and the launch of the persistent kernel.
+// group_gemm.cu -- C-ABI entry points nvfp4_group_gemm and
+// nvfp4_group_gemm_noalloc: validation, the per-call tile plan, the kernel
+// configuration for the shape class, tensor maps and the launches of the
+// persistent kernel.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -13,25 +15,56 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBN = 128;
 constexpr int kMaxDim = 1 << 20;
 constexpr int kMaxGroupsPerCall = 4096;
 constexpr long long kMaxTilesPerLaunch = 1ll << 30;
+constexpr int kMaxDevices = 64;
+
+enum Kind : int { kKindStream = 0, kKindWide = 1, kKindCompute = 2, kKindWide4 = 3, kNumKinds = 4 };
+
+template <class Cfg>
+void launch_kind(const GemmParams &P, int grid, cudaStream_t s)
+{
+    nvfp4_group_gemm_kernel<Cfg><<<grid, kThreads, Cfg::kSmemBytes, s>>>(P);
+}
+
+struct KindInfo {
+    int bn;
+    int chunks;     // 128-byte K chunks per row per stage
+    int epi_cols;
+    int smem;
+    const void *fn;
+    void (*launch)(const GemmParams &, int, cudaStream_t);
+};
+
+template <class Cfg>
+KindInfo make_kind()
+{
+    return KindInfo{Cfg::BN, Cfg::kChunks, Cfg::kEpiCols, Cfg::kSmemBytes,
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg>), &launch_kind<Cfg>};
+}
+
+const KindInfo &kind_info(int k)
+{
+    static const KindInfo table[kNumKinds] = {make_kind<CfgStream>(), make_kind<CfgWide>(),
+                                              make_kind<CfgCompute>(), make_kind<CfgWide4>()};
+    return table[k];
+}
 
 std::mutex g_attr_mu;
-bool g_attr_set[64];
+bool g_attr_set[kMaxDevices][kNumKinds];
 
-int ensure_kernel_attributes(int dev)
+int ensure_kernel_attributes(int dev, int kind)
 {
     std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev < 0 || dev >= 64)
+    if (dev < 0 || dev >= kMaxDevices)
         return NVFP4_ERR_UNSUPPORTED;
-    if (!g_attr_set[dev]) {
-        if (cudaFuncSetAttribute(nvfp4_group_gemm_kernel<kBN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GemmConfig<kBN>::kSmemBytes) != cudaSuccess)
+    if (!g_attr_set[dev][kind]) {
+        const KindInfo &ki = kind_info(kind);
+        if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) !=
+            cudaSuccess)
             return NVFP4_ERR_CUDA;
-        g_attr_set[dev] = true;
+        g_attr_set[dev][kind] = true;
     }
     return NVFP4_OK;
 }
@@ -52,30 +85,8 @@ int validate_group(const GroupDesc &g)
     return NVFP4_OK;
 }
 
-// L2 policy for B and its scales: B is streamed once per M-tile of its
-// group, and the M-tiles of one B strip run side by side, so the default
-// keeps B at normal priority (A and the A scales are kept: evict_last)
-int choose_b_policy()
+int validate_call(const GroupDesc *groups, int num_groups)
 {
-    const int o = b_policy_override();
-    return (o >= 0 && o <= 2) ? o : 0;
-}
-
-int launch_chunk(GemmParams &P, int sm_count, cudaStream_t stream)
-{
-    if (P.total_tiles == 0)
-        return NVFP4_OK;
-    const int grid = P.total_tiles < sm_count ? P.total_tiles : sm_count;
-    nvfp4_group_gemm_kernel<kBN><<<grid, kThreads, GemmConfig<kBN>::kSmemBytes, stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
-}
-
-}  // namespace
-}  // namespace nvfp4
-
-extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream)
-{
-    using namespace nvfp4;
     if (!groups || num_groups < 1)
         return NVFP4_ERR_INVALID_ARGUMENT;
     if (num_groups > kMaxGroupsPerCall)
@@ -85,70 +96,155 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
         if (rc != NVFP4_OK)
             return rc;
     }
-    DeviceState *dev = nullptr;
-    int rc = current_device(&dev);
-    if (rc != NVFP4_OK)
-        return rc;
-    int dev_id = 0;
-    cudaGetDevice(&dev_id);
-    rc = ensure_kernel_attributes(dev_id);
-    if (rc != NVFP4_OK)
-        return rc;
+    return NVFP4_OK;
+}
 
-    // Encode every tensor map before the first launch so that a rejected
-    // map launches nothing.  Up to kMaxGroups non-empty groups share one
-    // launch; a call with more is split into several launches on `stream`.
-    // The parameter blocks live in a per-thread vector whose capacity is
-    // kept, so steady-state calls allocate nothing.
+// Kernel configuration of a call.  BN = 256 tiles (CfgWide) halve the A
+// re-reads and the TMA operations per output byte, which the measurements on
+// GB300 show matters for every shape here; they need every N to be a multiple
+// of 256 (a B tile takes two whole 128-row scale blocks).  Otherwise BN = 128
+// with 512-K stages (CfgStream).  NVFP4_GEMM_KIND overrides the choice.
+int choose_kind(const GroupDesc *groups, int n)
+{
+    const int forced = env_int("NVFP4_GEMM_KIND", -1);
+    bool all_n256 = true;
+    for (int i = 0; i < n; ++i)
+        if (groups[i].M > 0)
+            all_n256 = all_n256 && (groups[i].N % 256 == 0);
+    if (forced == kKindWide || forced == kKindWide4)
+        return all_n256 ? forced : kKindStream;
+    if (forced == kKindStream || forced == kKindCompute)
+        return forced;
+    return all_n256 ? kKindWide : kKindStream;
+}
+
+// L2 policy for B and its scales: B is streamed once per M-tile of its
+// group, and the M-tiles of one B strip run side by side, so the default
+// keeps B at normal priority (A and the A scales are kept: evict_last)
+int choose_b_policy()
+{
+    const int o = b_policy_override();
+    return (o >= 0 && o <= 2) ? o : 0;
+}
+
+// L2 prefetch distance (stages ahead of the ring) for B; off unless asked
+int choose_prefetch()
+{
+    const int forced = env_int("NVFP4_PF_STAGES", -1);
+    return forced >= 0 ? forced : 0;
+}
+
+// launches a call needs for tile width bn (one per 32 non-empty groups,
+// more only past 2^30 tiles); must agree with plan_and_launch
+int count_launches(const GroupDesc *groups, int num_groups, int bn)
+{
+    int launches = 0, in_launch = 0;
+    long long tiles_in_launch = 0;
+    for (int i = 0; i < num_groups; ++i) {
+        const GroupDesc &g = groups[i];
+        if (g.M == 0)
+            continue;
+        const long long tiles =
+            (long long)((g.M + kBM - 1) / kBM) * (long long)((g.N + bn - 1) / bn);
+        if (launches == 0 || in_launch == kMaxGroups || tiles_in_launch + tiles > kMaxTilesPerLaunch) {
+            ++launches;
+            in_launch = 0;
+            tiles_in_launch = 0;
+        }
+        ++in_launch;
+        tiles_in_launch += tiles;
+    }
+    return launches;
+}
+
+// Plan and launch a validated call.  `err_for_launch(l)` gives the status
+// words of launch l.  Tensor maps of every launch are encoded before the
+// first launch, so a rejected map launches nothing.  The parameter blocks
+// live in a per-thread vector whose capacity is kept between calls.
+template <class ErrFn>
+int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int sm_count,
+                    int kind, ErrFn err_for_launch)
+{
     static thread_local std::vector<GemmParams> plist;
+    const KindInfo &ki = kind_info(kind);
     const int b_policy = choose_b_policy();
+    const int pf = choose_prefetch();
     const unsigned long long timeout = wait_timeout_ns();
     const int drop = debug_drop_stage();
-    auto fresh = [&]() -> GemmParams & {
-        plist.emplace_back();
-        GemmParams &P = plist.back();
-        std::memset(&P, 0, sizeof(P));
-        P.err = dev->err;
-        P.timeout_ns = timeout;
-        P.b_policy = b_policy;
-        P.debug_drop_stage = drop;
-        return P;
-    };
+    const CUtensorMapSwizzle c_swizzle =
+        ki.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     plist.clear();
+    int rc = NVFP4_OK;
     for (int i = 0; i < num_groups && rc == NVFP4_OK; ++i) {
         const GroupDesc &g = groups[i];
         if (g.M == 0)
             continue;
         const int grid_m = (g.M + kBM - 1) / kBM;
-        const int grid_n = (g.N + kBN - 1) / kBN;
+        const int grid_n = (g.N + ki.bn - 1) / ki.bn;
         const long long tiles = (long long)grid_m * grid_n;
         if (plist.empty() || plist.back().num_groups == kMaxGroups ||
-            plist.back().total_tiles + tiles > kMaxTilesPerLaunch)
-            fresh();
-        GemmParams *P = &plist.back();
-        const int j = P->num_groups;
-        const uint64_t kbytes = (uint64_t)g.K / 2;
-        rc = encode_map_2d(&P->tmA[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.A, kbytes, (uint64_t)g.M,
-                           kbytes, kBK / 2, kBM);
+            plist.back().total_tiles + tiles > kMaxTilesPerLaunch) {
+            plist.emplace_back();
+            GemmParams &P = plist.back();
+            std::memset(&P, 0, sizeof(P));
+            P.err = err_for_launch((int)plist.size() - 1);
+            P.timeout_ns = timeout;
+            P.b_policy = b_policy;
+            P.pf_stages = pf;
+            P.debug_drop_stage = drop;
+        }
+        GemmParams &P = plist.back();
+        const int j = P.num_groups;
+        rc = encode_map_operand(&P.tmA[j], g.A, (uint64_t)g.M, (uint64_t)g.K, kBM, ki.chunks);
         if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P->tmB[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.B, kbytes,
-                               (uint64_t)g.N, kbytes, kBK / 2, kBN);
+            rc = encode_map_operand(&P.tmB[j], g.B, (uint64_t)g.N, (uint64_t)g.K, ki.bn, ki.chunks);
         if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P->tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
-                               (uint64_t)g.M, (uint64_t)g.N * 2, 64, 32);
-        P->sfa[j] = static_cast<const uint8_t *>(g.SFA);
-        P->sfb[j] = static_cast<const uint8_t *>(g.SFB);
-        P->M[j] = g.M;
-        P->N[j] = g.N;
-        P->kiters[j] = g.K / kBK;
-        P->grid_m[j] = grid_m;
-        P->total_tiles += (int)tiles;
-        P->tile_end[j] = P->total_tiles;
-        P->num_groups = j + 1;
+            rc = encode_map_2d(&P.tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
+                               (uint64_t)g.M, (uint64_t)g.N * 2, ki.epi_cols, 32, c_swizzle);
+        P.sfa[j] = static_cast<const uint8_t *>(g.SFA);
+        P.sfb[j] = static_cast<const uint8_t *>(g.SFB);
+        P.M[j] = g.M;
+        P.N[j] = g.N;
+        P.kchunks[j] = g.K / kChunkK;
+        P.grid_m[j] = grid_m;
+        P.total_tiles += (int)tiles;
+        P.tile_end[j] = P.total_tiles;
+        P.num_groups = j + 1;
     }
-    for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l)
-        rc = launch_chunk(plist[l], dev->sm_count, stream);
+    for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
+        const GemmParams &P = plist[l];
+        const int grid = P.total_tiles < sm_count ? P.total_tiles : sm_count;
+        ki.launch(P, grid, stream);
+        if (cudaGetLastError() != cudaSuccess)
+            rc = NVFP4_ERR_CUDA;
+    }
     return rc;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream)
+{
+    using namespace nvfp4;
+    int rc = validate_call(groups, num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    const int kind = choose_kind(groups, num_groups);
+    if (count_launches(groups, num_groups, kind_info(kind).bn) == 0)
+        return NVFP4_OK;
+    DeviceState *dev = nullptr;
+    rc = current_device(&dev);
+    if (rc != NVFP4_OK)
+        return rc;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    rc = ensure_kernel_attributes(dev_id, kind);
+    if (rc != NVFP4_OK)
+        return rc;
+    uint32_t *err = dev->err;
+    return plan_and_launch(groups, num_groups, stream, dev->sm_count, kind,
+                           [err](int) { return err; });
 }
 
 // ---------------------------------------------------------------------------
@@ -176,17 +272,17 @@ struct NoAllocDevice {
     uint32_t *scratch;  // device address of g_noalloc_scratch on this device
 };
 std::mutex g_noalloc_mu;
-NoAllocDevice g_noalloc_dev[64];
+NoAllocDevice g_noalloc_dev[kMaxDevices];
 
 // One-time set-up for the current device (the first call on each device):
-// capability check, the kernel's shared-memory attribute and the device
-// address of the static scratch array.  None of these allocates.
+// capability check and the device address of the static scratch array.
+// Neither allocates.
 int noalloc_device(NoAllocDevice **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    if (dev < 0 || dev >= 64)
+    if (dev < 0 || dev >= kMaxDevices)
         return NVFP4_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     NoAllocDevice &d = g_noalloc_dev[dev];
@@ -198,9 +294,6 @@ int noalloc_device(NoAllocDevice **out)
             return NVFP4_ERR_CUDA;
         if (!(major == 10 && minor == 3))
             return NVFP4_ERR_UNSUPPORTED;
-        int rc = ensure_kernel_attributes(dev);
-        if (rc != NVFP4_OK)
-            return rc;
         uint32_t *ptr = nullptr;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_scratch) != cudaSuccess ||
             ptr == nullptr)
@@ -220,96 +313,31 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
                                         cudaStream_t stream)
 {
     using namespace nvfp4;
-    if (!groups || num_groups < 1)
-        return NVFP4_ERR_INVALID_ARGUMENT;
-    if (num_groups > kMaxGroupsPerCall)
-        return NVFP4_ERR_TOO_MANY;
-    // pass 1: validate, and count the launches (each needs its own two
-    // status words of the static scratch)
-    int launches = 0, in_launch = 0;
-    long long tiles_in_launch = 0;
-    for (int i = 0; i < num_groups; ++i) {
-        int rc = validate_group(groups[i]);
-        if (rc != NVFP4_OK)
-            return rc;
-        const GroupDesc &g = groups[i];
-        if (g.M == 0)
-            continue;
-        const long long tiles =
-            (long long)((g.M + kBM - 1) / kBM) * (long long)((g.N + kBN - 1) / kBN);
-        if (launches == 0 || in_launch == kMaxGroups || tiles_in_launch + tiles > kMaxTilesPerLaunch) {
-            ++launches;
-            in_launch = 0;
-            tiles_in_launch = 0;
-        }
-        ++in_launch;
-        tiles_in_launch += tiles;
-    }
+    int rc = validate_call(groups, num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    const int kind = choose_kind(groups, num_groups);
+    // each launch needs its own two status words of the static scratch
+    const int launches = count_launches(groups, num_groups, kind_info(kind).bn);
     if (launches == 0)
         return NVFP4_OK;
     if (launches > kNoAllocMaxLaunches)
         return NVFP4_ERR_TOO_MANY;   // more than 32 launches' worth (> 1024 non-empty groups)
 
     NoAllocDevice *dev = nullptr;
-    int rc = noalloc_device(&dev);
+    rc = noalloc_device(&dev);
+    if (rc != NVFP4_OK)
+        return rc;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    rc = ensure_kernel_attributes(dev_id, kind);
     if (rc != NVFP4_OK)
         return rc;
     // the status words must start at zero; the array keeps the previous
     // call's contents otherwise
     if (cudaMemsetAsync(dev->scratch, 0, sizeof(uint32_t) * 2 * launches, stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-
-    // pass 2: one parameter block at a time (launch copies it), launched as
-    // soon as its groups are encoded
-    static thread_local GemmParams P;
-    const int b_policy = choose_b_policy();
-    const unsigned long long timeout = wait_timeout_ns();
-    const int drop = debug_drop_stage();
-    int launch = 0;
-    bool open = false;
-    for (int i = 0; i < num_groups && rc == NVFP4_OK; ++i) {
-        const GroupDesc &g = groups[i];
-        if (g.M == 0)
-            continue;
-        const int grid_m = (g.M + kBM - 1) / kBM;
-        const int grid_n = (g.N + kBN - 1) / kBN;
-        const long long tiles = (long long)grid_m * grid_n;
-        if (open && (P.num_groups == kMaxGroups || P.total_tiles + tiles > kMaxTilesPerLaunch)) {
-            rc = launch_chunk(P, dev->sm_count, stream);
-            open = false;
-            ++launch;
-            if (rc != NVFP4_OK)
-                break;
-        }
-        if (!open) {
-            std::memset(&P, 0, sizeof(P));
-            P.err = dev->scratch + 2 * launch;
-            P.timeout_ns = timeout;
-            P.b_policy = b_policy;
-            P.debug_drop_stage = drop;
-            open = true;
-        }
-        const int j = P.num_groups;
-        const uint64_t kbytes = (uint64_t)g.K / 2;
-        rc = encode_map_2d(&P.tmA[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.A, kbytes, (uint64_t)g.M,
-                           kbytes, kBK / 2, kBM);
-        if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P.tmB[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.B, kbytes,
-                               (uint64_t)g.N, kbytes, kBK / 2, kBN);
-        if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P.tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
-                               (uint64_t)g.M, (uint64_t)g.N * 2, 64, 32);
-        P.sfa[j] = static_cast<const uint8_t *>(g.SFA);
-        P.sfb[j] = static_cast<const uint8_t *>(g.SFB);
-        P.M[j] = g.M;
-        P.N[j] = g.N;
-        P.kiters[j] = g.K / kBK;
-        P.grid_m[j] = grid_m;
-        P.total_tiles += (int)tiles;
-        P.tile_end[j] = P.total_tiles;
-        P.num_groups = j + 1;
-    }
-    if (rc == NVFP4_OK && open)
-        rc = launch_chunk(P, dev->sm_count, stream);
-    return rc;
+    uint32_t *scratch = dev->scratch;
+    return plan_and_launch(groups, num_groups, stream, dev->sm_count, kind,
+                           [scratch](int l) { return scratch + 2 * l; });
 }

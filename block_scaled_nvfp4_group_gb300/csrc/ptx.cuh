@@ -94,6 +94,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// 3-D tiled load global -> shared (box over several 128-byte K chunks)
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 prefetch of one 3-D tile (no shared memory involved)
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
+            tmap),
+        "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 // contiguous bulk load global -> shared (16-byte aligned, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar, uint64_t policy)

@@ -27,13 +27,14 @@ std::atomic<int> g_debug_drop{0};
 
 struct MapKey {
     const void *ptr;
-    uint64_t dim0, dim1, stride1;
-    uint32_t box0, box1;
-    int dtype;
+    uint64_t dim0, dim1, dim2, stride1, stride2;
+    uint32_t box0, box1, box2;
+    int rank, dtype, swizzle;
     bool operator==(const MapKey &o) const
     {
-        return ptr == o.ptr && dim0 == o.dim0 && dim1 == o.dim1 && stride1 == o.stride1 &&
-               box0 == o.box0 && box1 == o.box1 && dtype == o.dtype;
+        return ptr == o.ptr && dim0 == o.dim0 && dim1 == o.dim1 && dim2 == o.dim2 &&
+               stride1 == o.stride1 && stride2 == o.stride2 && box0 == o.box0 && box1 == o.box1 &&
+               box2 == o.box2 && rank == o.rank && dtype == o.dtype && swizzle == o.swizzle;
     }
 };
 struct MapKeyHash {
@@ -45,9 +46,12 @@ struct MapKeyHash {
         };
         mix(k.dim0);
         mix(k.dim1);
+        mix(k.dim2);
         mix(k.stride1);
+        mix(k.stride2);
         mix((uint64_t)k.box0 << 32 | k.box1);
-        mix((uint64_t)k.dtype);
+        mix((uint64_t)k.box2 << 32 | (uint64_t)k.rank << 16 | (uint64_t)k.dtype << 8 |
+            (uint64_t)k.swizzle);
         return (size_t)h;
     }
 };
@@ -111,10 +115,10 @@ int current_device(DeviceState **out)
     return d.supported ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
 }
 
-int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t dim0,
-                  uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1)
+namespace {
+
+int encode_map(CUtensorMap *out, const MapKey &key)
 {
-    const MapKey key{ptr, dim0, dim1, stride1_bytes, box0, box1, (int)dtype};
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
     if (it != g_maps.end()) {
@@ -124,12 +128,13 @@ int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, 
     int rc = load_encoder();
     if (rc != NVFP4_OK)
         return rc;
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride1_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(out, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const cuuint64_t dims[3] = {key.dim0, key.dim1, key.dim2};
+    const cuuint64_t strides[2] = {key.stride1, key.stride2};
+    const cuuint32_t box[3] = {key.box0, key.box1, key.box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(out, (CUtensorMapDataType)key.dtype, (cuuint32_t)key.rank,
+                          const_cast<void *>(key.ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)key.swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return NVFP4_ERR_INVALID_ARGUMENT;
@@ -139,13 +144,28 @@ int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, 
     return NVFP4_OK;
 }
 
+}  // namespace
+
+int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t dim0,
+                  uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                  CUtensorMapSwizzle swizzle)
+{
+    const MapKey key{ptr, dim0, dim1, 1, stride1_bytes, 0, box0, box1, 1, 2, (int)dtype, (int)swizzle};
+    return encode_map(out, key);
+}
+
+int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K,
+                       uint32_t box_rows, uint32_t box_chunks)
+{
+    const MapKey key{ptr,   128, rows,     K / 256,    K / 2, 128, 128, box_rows, box_chunks, 3,
+                     (int)CU_TENSOR_MAP_DATA_TYPE_UINT8, (int)CU_TENSOR_MAP_SWIZZLE_128B};
+    return encode_map(out, key);
+}
+
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 int debug_drop_stage() { return g_debug_drop.load(std::memory_order_relaxed); }
-int b_policy_override()
-{
-    static const int v = read_env_int("NVFP4_B_POLICY", -1);
-    return v;
-}
+int b_policy_override() { return read_env_int("NVFP4_B_POLICY", -1); }
+int env_int(const char *name, int fallback) { return read_env_int(name, fallback); }
 
 }  // namespace nvfp4
 

@@ -21,14 +21,26 @@ struct DeviceState {
 int current_device(DeviceState **out);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point, with a
-// cache keyed on every argument that varies.  2-D, 128-byte swizzle, 256-byte
-// L2 promotion, zero fill out of bounds.  Returns an NVFP4_* code.
+// cache keyed on every argument that varies.  2-D, 256-byte L2 promotion,
+// zero fill out of bounds.  Returns an NVFP4_* code.
 int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t dim0,
-                  uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1);
+                  uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                  CUtensorMapSwizzle swizzle);
+
+// K-major packed FP4 operand [rows][K/2] bytes as a 3-D uint8 tensor
+// {128 B, rows, K/256} (strides K/2 and 128 bytes), box {128, box_rows,
+// box_chunks}, 128-byte swizzle: one load brings box_chunks consecutive
+// 128-byte pieces of every row.
+int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K,
+                       uint32_t box_rows, uint32_t box_chunks);
 
 unsigned long long wait_timeout_ns();
 int debug_drop_stage();
 int b_policy_override();   // -1 = use the built-in choice
+// tuning and debug knobs from the environment, read at every call:
+// NVFP4_GEMM_KIND (0 stream, 1 wide, 2 compute, 3 wide with 256-K stages),
+// NVFP4_PF_STAGES, NVFP4_B_POLICY (0 normal, 1 evict_first, 2 evict_last)
+int env_int(const char *name, int fallback);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

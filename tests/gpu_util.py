@@ -33,3 +33,34 @@ def compare_fp16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
                              f"first at {idx.tolist()}: gpu {g[tuple(idx[0])]} "
                              f"oracle {r[tuple(idx[0])]}")
+
+
+KINDS = {"stream": 0, "wide": 1, "compute": 2, "wide4": 3}
+
+
+class gemm_env:
+    """Force the GEMM configuration (and optionally the L2 prefetch distance)
+    through the library's environment knobs, restoring them afterwards."""
+
+    def __init__(self, kind=None, pf=None):
+        import os
+        self.os = os
+        self.vals = {"NVFP4_GEMM_KIND": None if kind is None else str(KINDS[kind]),
+                     "NVFP4_PF_STAGES": None if pf is None else str(pf)}
+        self.saved = {}
+
+    def __enter__(self):
+        for k, v in self.vals.items():
+            self.saved[k] = self.os.environ.get(k)
+            if v is None:
+                self.os.environ.pop(k, None)
+            else:
+                self.os.environ[k] = v
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            if v is None:
+                self.os.environ.pop(k, None)
+            else:
+                self.os.environ[k] = v

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import compare_fp16, require_gb300
+from gpu_util import compare_fp16, gemm_env, require_gb300
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
@@ -46,21 +46,38 @@ def test_small_single_tile():
     run_and_compare(workloads.make_groups([(128, 128, 256)], seed=1))
 
 
-def test_ragged_several_tiles():
+@pytest.mark.parametrize("kind", ["stream", "compute"])
+def test_ragged_several_tiles(kind):
     """Several M and N tiles per group, ragged tails in M and N, one-stage
-    and multi-stage K, an empty group in the middle."""
+    and multi-stage K (K % 512 == 256 too: a half last stage), an empty
+    group in the middle."""
     from block_scaled_nvfp4_group_gb300 import workloads
     shapes = [(200, 384, 1024), (77, 256, 512), (0, 256, 256), (1, 136, 256), (300, 520, 768),
               (129, 8, 2048)]
-    run_and_compare(workloads.make_groups(shapes, seed=2))
+    with gemm_env(kind):
+        run_and_compare(workloads.make_groups(shapes, seed=2))
 
 
-def test_more_stages_than_ring_and_many_tiles():
+@pytest.mark.parametrize("kind", ["wide", "wide4"])
+def test_wide_tiles_ragged_m(kind):
+    """BN = 256 tiles (two scale blocks per B tile), ragged M, several N
+    tiles, one- and multi-stage K, half last stages."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(77, 512, 1024), (300, 256, 512), (1, 768, 256), (129, 1024, 2304)]
+    with gemm_env(kind):
+        run_and_compare(workloads.make_groups(shapes, seed=21))
+
+
+@pytest.mark.parametrize("kind,pf", [("stream", 0), ("stream", 8), ("stream", 40), ("wide", 0),
+                                     ("wide", 8), ("wide4", 0), ("compute", 0)])
+def test_more_stages_than_ring_and_many_tiles(kind, pf):
     """K large enough to wrap the shared-memory ring several times per tile
-    and more tiles than SMs (persistent loop, both accumulator buffers)."""
+    and more tiles than SMs (persistent loop, both accumulator buffers), with
+    the L2 prefetch of B off, on, and running across tile boundaries."""
     from block_scaled_nvfp4_group_gb300 import workloads
     shapes = [(384, 2048, 4096), (256, 4096, 2560)]
-    run_and_compare(workloads.make_groups(shapes, seed=3))
+    with gemm_env(kind, pf):
+        run_and_compare(workloads.make_groups(shapes, seed=3))
 
 
 def test_more_groups_than_one_launch():
@@ -137,14 +154,18 @@ def test_workload_quantized():
     run_and_compare(workloads.make_workload("quantized").groups)
 
 
-def test_workload_moe_down():
+@pytest.mark.parametrize("kind", [None, "stream", "wide4", "compute"])
+def test_workload_moe_down(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
-    run_and_compare(workloads.make_workload("moe_down").groups)
+    with gemm_env(kind):
+        run_and_compare(workloads.make_workload("moe_down").groups)
 
 
-def test_workload_moe_gate_up():
+@pytest.mark.parametrize("kind", [None, "stream", "wide4", "compute"])
+def test_workload_moe_gate_up(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
-    run_and_compare(workloads.make_workload("moe_gate_up").groups)
+    with gemm_env(kind):
+        run_and_compare(workloads.make_workload("moe_gate_up").groups)
 
 
 def test_workload_square_sampled_rows():
