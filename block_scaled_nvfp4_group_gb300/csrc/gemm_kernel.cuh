@@ -2,27 +2,26 @@
 // sm_103a (GB300).
 //
 // One CTA per SM walks a flat list of output tiles of every group
-// (tile t, t + gridDim.x, ...).  Eight warps, four roles:
+// (tile t, t + gridDim.x, ...).  Warps and roles:
 //   warps 0-3  epilogue: tensor memory -> registers (tcgen05.ld), FP32 ->
 //              FP16 (round to nearest even), a swizzled shared-memory tile
 //              per warp and a TMA tensor store, which writes whole row
 //              segments and clips rows >= M and columns >= N;
-//   warp 4     B producer: per stage of BK K-elements, one 3-D TMA load of
-//              the B tile [BN rows x BK/2 bytes] (128-byte swizzle, BK/256
-//              chunks of 128 bytes per row) and bulk copies of the matching
-//              tiled B scale atoms;
-//   warp 6     A producer: the same for the A tile [128 x BK/2 bytes] and
-//              its scales.  Two issuing warps and multi-chunk boxes keep the
-//              TMA issue rate (a few operations per microsecond per issuing
-//              thread on GB300) from bounding the stream;
-//   warp 5     MMA issuer (one thread): tcgen05.cp of the stage's scale
+//   warps 5..  producer pairs: per stage of BK K-elements, the B warp of a
+//              pair issues one 3-D TMA load of the B tile [BN rows x BK/2
+//              bytes] (128-byte swizzle, BK/256 chunks of 128 bytes per row)
+//              and bulk copies of the matching tiled B scale atoms, the A warp
+//              the same for the A tile [128 x BK/2 bytes] and its scales.  The
+//              pairs take the stages round robin: on GB300 the TMA operations
+//              of one issuing thread complete roughly one after another, so
+//              several issuing warps keep more loads in flight;
+//   warp 4     MMA issuer (one thread): tcgen05.cp of the stage's scale
 //              atoms into tensor memory, BK/64
 //              tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
 //              per stage into an FP32 accumulator (two of them when BN=128),
-//              and tcgen05.commit to free the stage / hand the accumulator on;
-//   warp 7     idle.
+//              and tcgen05.commit to free the stage / hand the accumulator on.
 // The ring of STAGES shared-memory slots is guarded by mbarrier full/empty
-// pairs (full counts the two producers' arrivals plus the copied bytes).
+// pairs (full counts the A and B producers' arrivals plus the copied bytes).
 // With two accumulators the epilogue of tile t overlaps the MMAs of t+1;
 // with one, the producers still stream tile t+1's stages meanwhile.
 //
@@ -51,10 +50,8 @@ constexpr int kBM = 128;           // MMA M, rows of A per tile
 constexpr int kChunkK = 256;       // K elements per 128-byte chunk of a row
 constexpr int kMmaK = 64;          // K elements per tcgen05.mma (FP4)
 constexpr int kMaxGroups = 32;     // groups per launch (param block)
-constexpr int kThreads = 256;      // 4 epilogue warps, B producer, MMA, A producer, idle
-constexpr int kProducerBWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kProducerAWarp = 6;
+constexpr int kMmaWarp = 4;        // MMA issuer; also allocates / frees tensor memory
+constexpr int kFirstProducerWarp = 5;
 constexpr int kSmemLimit = 232448; // 227 KiB per CTA
 
 // error word bits (device_err[0]); device_err[1] records who expired first
@@ -85,12 +82,20 @@ struct GemmParams {
 
 // BN: tile width; BK: K elements per stage (256 or 512); STAGES: ring depth;
 // EPI_COLS: columns per epilogue store (32 or 64); EPI_BUFS: staging
-// buffers per epilogue warp (1 or 2)
-template <int BN_, int BK_, int STAGES_, int EPI_COLS_, int EPI_BUFS_>
+// buffers per epilogue warp (1 or 2); PRODUCERS: producer pairs (one A and
+// one B warp each) taking the stages round robin
+template <int BN_, int BK_, int STAGES_, int EPI_COLS_, int EPI_BUFS_, int PRODUCERS_>
 struct GemmConfig {
     static constexpr int BN = BN_;
     static constexpr int BK = BK_;
     static constexpr int kStages = STAGES_;
+    static constexpr int kProducers = PRODUCERS_;
+    static_assert(kProducers >= 1 && kProducers <= 4, "1 to 4 producer pairs");
+    // every ring slot must always be served by the same producer pair, so
+    // that a producer's last issue of a slot is that slot's last phase (the
+    // drain at the end waits on it)
+    static_assert(STAGES_ % PRODUCERS_ == 0, "stages must be a multiple of the producer pairs");
+    static constexpr int kThreads = 32 * (kFirstProducerWarp + 2 * kProducers);
     static constexpr int kEpiCols = EPI_COLS_;
     static constexpr int kEpiBufs = EPI_BUFS_;
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
@@ -259,11 +264,14 @@ struct StageCursor {
 };
 
 // One producer role: `IS_B` selects B (tile width BN, scales of BN/128 row
-// blocks) or A (128 rows, scales of one row block).  Arrives once per stage
-// on full[stage] with the bytes it will deliver.
+// blocks) or A (128 rows, scales of one row block); the role serves the
+// stages q of this CTA's stage sequence with q % kProducers == cls.  The TMA
+// operations one thread issues complete about one after another, so the
+// stages are spread over several producer warps.  Arrives once per served
+// stage on full[slot] with the bytes it will deliver.
 template <class Cfg, bool IS_B>
 __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base, uint32_t bar0,
-                                              const WaitCtx &wctx)
+                                              const WaitCtx &wctx, int cls)
 {
     constexpr int S = Cfg::kStages;
     constexpr int ROWS = IS_B ? Cfg::BN : kBM;
@@ -278,14 +286,13 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
                                  : p.b_policy == 2 ? ptx::policy_evict_last()
                                                    : ptx::policy_evict_normal())
                               : ptx::policy_evict_last();
-    StageCursor<Cfg::BK> pf;
-    pf.start(p, IS_B ? (int)blockIdx.x : p.total_tiles);   // the A producer never prefetches
+    StageCursor<Cfg::BK> pf;   // only the first B producer prefetches
+    pf.start(p, (IS_B && cls == 0) ? (int)blockIdx.x : p.total_tiles);
     for (int i = 0; i < p.pf_stages && pf.valid(p); ++i) {  // run pf_stages ahead of the loads
         ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks, pol);
         pf.advance(p);
     }
-    int stage = 0;
-    uint32_t phase = 0;
+    uint32_t q = 0;   // position in this CTA's sequence of stages
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
     int g = 0;
@@ -297,13 +304,16 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
         const int row0 = IS_B ? tc.bn * Cfg::BN : tc.bm * kBM;
         const CUtensorMap *tm = IS_B ? &p.tmB[tc.g] : &p.tmA[tc.g];
         const uint8_t *sf = (IS_B ? p.sfb[tc.g] : p.sfa[tc.g]) + (size_t)(row0 / 128) * kblk * 512;
-        for (int it = 0; it < nst; ++it) {
+        for (int it = 0; it < nst; ++it, ++q) {
+            if ((int)(q % Cfg::kProducers) != cls)
+                continue;
+            const int stage = (int)(q % S);
+            const uint32_t phase = (q / S) & 1u;
             if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx, kRoleProducer)) {
                 ok = false;
                 break;
             }
-            const bool drop = IS_B && p.debug_drop_stage && blockIdx.x == 0 &&
-                              t == (int)blockIdx.x && it == 0;
+            const bool drop = IS_B && p.debug_drop_stage && blockIdx.x == 0 && q == 0;
             if (!drop) {
                 const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
                 const uint32_t st = base + stage * Cfg::kStageBytes;
@@ -319,14 +329,10 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
-            if (pf.valid(p)) {
+            for (int i = 0; i < Cfg::kProducers && pf.valid(p); ++i) {
                 ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks,
                                      pol);
                 pf.advance(p);
-            }
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
             }
         }
     }
@@ -341,7 +347,7 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
 }
 
 template <class Cfg>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     nvfp4_group_gemm_kernel(const __grid_constant__ GemmParams p)
 {
     constexpr int BN = Cfg::BN;
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(full_bar(s), 2);   // one arrival per producer
+            ptx::mbar_init(full_bar(s), 2);   // one A and one B producer per stage
             ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
-    if (warp == kProducerBWarp) {
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(tmem_slot, Cfg::kTmemCols);
         ptx::tmem_relinquish();
         ptx::tc_fence_before();
@@ -390,12 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};
     const int total = p.total_tiles;
 
-    if (warp == kProducerBWarp) {
-        if (lane == 0)
-            producer_role<Cfg, true>(p, base, bar0, wctx);
-    } else if (warp == kProducerAWarp) {
-        if (lane == 0)
-            producer_role<Cfg, false>(p, base, bar0, wctx);
+    if (warp >= kFirstProducerWarp) {
+        // producer warps: A, B, A, B, ... for stage classes 0, 0, 1, 1, ...
+        const int pw = warp - kFirstProducerWarp;
+        if (lane == 0) {
+            if (pw & 1)
+                producer_role<Cfg, true>(p, base, bar0, wctx, pw >> 1);
+            else
+                producer_role<Cfg, false>(p, base, bar0, wctx, pw >> 1);
+        }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
@@ -571,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == kProducerBWarp) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
@@ -580,18 +589,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Kernel configurations, chosen per call by the host (group_gemm.cu).
-//   CfgStream:  HBM-bound shapes, BN = 128 -- 512-K stages (256 contiguous
-//               bytes per row per load), 3 stages, two accumulators, one
-//               2 KiB staging buffer per epilogue warp
-//   CfgWide:    BN = 256 -- half the A re-reads, 512-K stages, 2 stages, one
-//               accumulator
-//   CfgWide4:   BN = 256 with 256-K stages, 4 stages
-//   CfgCompute: BN = 128, 256-K stages, 5 stages, two 4 KiB staging buffers
-//               per warp (64-column stores) so the epilogue keeps up
+//   CfgStream:  BN = 128, 512-K stages (256 contiguous bytes per row per
+//               load), 3 stages, two accumulators, one 2 KiB staging buffer
+//               per epilogue warp
+//   CfgWide:    BN = 256 -- half the A re-reads -- 256-K stages, 4 stages,
+//               one accumulator
+//   CfgWide512: BN = 256 with 512-K stages, 2 stages
+//   CfgCompute: BN = 128, 256-K stages, 4 stages, two 4 KiB staging buffers
+//               per warp (64-column stores)
+// The last parameter is the number of producer pairs.
 // ---------------------------------------------------------------------------
-using CfgStream = GemmConfig<128, 512, 3, 32, 1>;
-using CfgWide = GemmConfig<256, 512, 2, 32, 1>;
-using CfgWide4 = GemmConfig<256, 256, 4, 32, 1>;
-using CfgCompute = GemmConfig<128, 256, 5, 64, 2>;
+using CfgStream = GemmConfig<128, 512, 3, 32, 1, 3>;
+using CfgWide = GemmConfig<256, 256, 4, 32, 1, 4>;
+using CfgWide512 = GemmConfig<256, 512, 2, 32, 1, 2>;
+using CfgCompute = GemmConfig<128, 256, 4, 64, 2, 4>;
+using CfgWideP1 = GemmConfig<256, 256, 4, 32, 1, 1>;
+using CfgWideP2 = GemmConfig<256, 256, 4, 32, 1, 2>;
 
 }  // namespace nvfp4

@@ -20,12 +20,25 @@ constexpr int kMaxGroupsPerCall = 4096;
 constexpr long long kMaxTilesPerLaunch = 1ll << 30;
 constexpr int kMaxDevices = 64;
 
-enum Kind : int { kKindStream = 0, kKindWide = 1, kKindCompute = 2, kKindWide4 = 3, kNumKinds = 4 };
+enum Kind : int {
+    kKindStream = 0,
+    kKindWide = 1,
+    kKindCompute = 2,
+    kKindWide512 = 3,
+    kKindWideP1 = 4,
+    kKindWideP2 = 5,
+    kNumKinds = 6
+};
+
+bool needs_n256(int kind)
+{
+    return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP1 || kind == kKindWideP2;
+}
 
 template <class Cfg>
 void launch_kind(const GemmParams &P, int grid, cudaStream_t s)
 {
-    nvfp4_group_gemm_kernel<Cfg><<<grid, kThreads, Cfg::kSmemBytes, s>>>(P);
+    nvfp4_group_gemm_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(P);
 }
 
 struct KindInfo {
@@ -46,8 +59,9 @@ KindInfo make_kind()
 
 const KindInfo &kind_info(int k)
 {
-    static const KindInfo table[kNumKinds] = {make_kind<CfgStream>(), make_kind<CfgWide>(),
-                                              make_kind<CfgCompute>(), make_kind<CfgWide4>()};
+    static const KindInfo table[kNumKinds] = {make_kind<CfgStream>(),  make_kind<CfgWide>(),
+                                              make_kind<CfgCompute>(), make_kind<CfgWide512>(),
+                                              make_kind<CfgWideP1>(),  make_kind<CfgWideP2>()};
     return table[k];
 }
 
@@ -111,10 +125,8 @@ int choose_kind(const GroupDesc *groups, int n)
     for (int i = 0; i < n; ++i)
         if (groups[i].M > 0)
             all_n256 = all_n256 && (groups[i].N % 256 == 0);
-    if (forced == kKindWide || forced == kKindWide4)
-        return all_n256 ? forced : kKindStream;
-    if (forced == kKindStream || forced == kKindCompute)
-        return forced;
+    if (forced >= 0 && forced < kNumKinds)
+        return (!needs_n256(forced) || all_n256) ? forced : kKindStream;
     return all_n256 ? kKindWide : kKindStream;
 }
 

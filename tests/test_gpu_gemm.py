@@ -58,7 +58,7 @@ def test_ragged_several_tiles(kind):
         run_and_compare(workloads.make_groups(shapes, seed=2))
 
 
-@pytest.mark.parametrize("kind", ["wide", "wide4"])
+@pytest.mark.parametrize("kind", ["wide", "wide512", "wide_p1", "wide_p2"])
 def test_wide_tiles_ragged_m(kind):
     """BN = 256 tiles (two scale blocks per B tile), ragged M, several N
     tiles, one- and multi-stage K, half last stages."""
@@ -69,7 +69,7 @@ def test_wide_tiles_ragged_m(kind):
 
 
 @pytest.mark.parametrize("kind,pf", [("stream", 0), ("stream", 8), ("stream", 40), ("wide", 0),
-                                     ("wide", 8), ("wide4", 0), ("compute", 0)])
+                                     ("wide", 8), ("wide512", 0), ("compute", 0)])
 def test_more_stages_than_ring_and_many_tiles(kind, pf):
     """K large enough to wrap the shared-memory ring several times per tile
     and more tiles than SMs (persistent loop, both accumulator buffers), with
@@ -154,14 +154,14 @@ def test_workload_quantized():
     run_and_compare(workloads.make_workload("quantized").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide4", "compute"])
+@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute"])
 def test_workload_moe_down(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
         run_and_compare(workloads.make_workload("moe_down").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide4", "compute"])
+@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute"])
 def test_workload_moe_gate_up(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
