@@ -16,7 +16,7 @@
 //              of one issuing thread complete roughly one after another, so
 //              several issuing warps keep more loads in flight;
 //   warp 4     MMA issuer (one thread): tcgen05.cp of the stage's scale
-//              atoms into tensor memory, BK/64
+//              atoms into the stage's own tensor-memory columns, BK/64
 //              tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
 //              per stage into an FP32 accumulator (two of them when BN=128),
 //              and tcgen05.commit to free the stage / hand the accumulator on.
@@ -119,11 +119,18 @@ struct GemmConfig {
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
-    // tensor memory: accumulators, then the scale columns of one stage
+    // tensor memory: accumulators, then one scale region per ring slot
+    // (SFA atoms, then SFB atoms): the copies for stage q+1 never write the
+    // columns the MMAs of stage q read, so they need not wait for them
     static constexpr int kTmemCols = 512;
-    static constexpr int kSfaCol = kAccBufs * BN;
-    static constexpr int kSfbCol = kSfaCol + 4 * kMmas;
-    static_assert(kSfbCol + 4 * kMmas * (BN / 128) <= kTmemCols, "tensor memory budget");
+    static constexpr int kSfCol0 = kAccBufs * BN;
+    static constexpr int kSfSlotCols = 4 * kMmas * (1 + BN / 128);
+    static_assert(kSfCol0 + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
+    static constexpr uint32_t sfa_col(int slot, int j) { return kSfCol0 + slot * kSfSlotCols + 4 * j; }
+    static constexpr uint32_t sfb_col(int slot, int j, int h)
+    {
+        return kSfCol0 + slot * kSfSlotCols + 4 * kMmas + 4 * (BN / 128) * j + 4 * h;
+    }
     // instruction descriptor (kind::mxf4nvf4): A and B E2M1 (format 1) at
     // bits 7 and 10, both K-major, N>>3 at bit 17, UE4M3 scales (bit 23 = 0),
     // M>>7 at bit 27, scale-factor data ids 0
@@ -438,12 +445,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < Cfg::kMmas; ++j) {
                         if (j < nk) {
-                            ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::kSfaCol + 4 * j,
+                            ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::sfa_col(stage, j),
                                                       desc_scale_atom(ssfa + 512 * j));
 #pragma unroll
                             for (int h = 0; h < BN / 128; ++h)
                                 ptx::tc_cp_32x128b_warpx4(
-                                    tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j + 4 * h,
+                                    tmem_base + Cfg::sfb_col(stage, j, h),
                                     desc_scale_atom(ssfb + Cfg::kMmas * 512 * h + 512 * j));
                         }
                     }
@@ -455,8 +462,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                             const uint32_t koff_b = (j / 4) * BN * 128 + (j % 4) * 32;
                             ptx::tc_mma_nvfp4(d_tmem, desc_operand_sw128(sa + koff_a),
                                               desc_operand_sw128(sb + koff_b), Cfg::kIdesc,
-                                              tmem_base + Cfg::kSfaCol + 4 * j,
-                                              tmem_base + Cfg::kSfbCol + 4 * (BN / 128) * j,
+                                              tmem_base + Cfg::sfa_col(stage, j),
+                                              tmem_base + Cfg::sfb_col(stage, j, 0),
                                               (it > 0 || j > 0) ? 1u : 0u);
                         }
                     }
