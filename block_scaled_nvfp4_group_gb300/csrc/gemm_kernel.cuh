@@ -7,7 +7,7 @@
 //              FP16 (round to nearest even), a swizzled shared-memory tile
 //              per warp and a TMA tensor store, which writes whole row
 //              segments and clips rows >= M and columns >= N;
-//   warps 5..  producer pairs: per stage of BK K-elements, the B warp of a
+//   warps 6..  producer pairs: per stage of BK K-elements, the B warp of a
 //              pair issues one 3-D TMA load of the B tile [BN rows x BK/2
 //              bytes] (128-byte swizzle, BK/256 chunks of 128 bytes per row)
 //              and bulk copies of the matching tiled B scale atoms, the A warp
@@ -15,8 +15,12 @@
 //              pairs take the stages round robin: on GB300 the TMA operations
 //              of one issuing thread complete roughly one after another, so
 //              several issuing warps keep more loads in flight;
-//   warp 4     MMA issuer (one thread): tcgen05.cp of the stage's scale
-//              atoms into the stage's own tensor-memory columns, BK/64
+//   warp 5     scale copier (one thread): once a stage has landed,
+//              tcgen05.cp of its scale atoms into the slot's own
+//              tensor-memory columns, then tcgen05.commit to sf_ready[slot]
+//              (copies issued by the MMA thread itself did not overlap the
+//              MMAs on GB300);
+//   warp 4     MMA issuer (one thread): after sf_ready[slot], BK/64
 //              tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
 //              per stage into an FP32 accumulator (two of them when BN=128),
 //              and tcgen05.commit to free the stage / hand the accumulator on.
@@ -51,14 +55,15 @@ constexpr int kChunkK = 256;       // K elements per 128-byte chunk of a row
 constexpr int kMmaK = 64;          // K elements per tcgen05.mma (FP4)
 constexpr int kMaxGroups = 32;     // groups per launch (param block)
 constexpr int kMmaWarp = 4;        // MMA issuer; also allocates / frees tensor memory
-constexpr int kFirstProducerWarp = 5;
+constexpr int kSfWarp = 5;         // scale copies shared -> tensor memory
+constexpr int kFirstProducerWarp = 6;
 constexpr int kSmemLimit = 232448; // 227 KiB per CTA
 
 // error word bits (device_err[0]); device_err[1] records who expired first
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrDrainTimeout = 2u;
 
-enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4 };
+enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4, kRoleSf = 5 };
 
 struct GemmParams {
     CUtensorMap tmA[kMaxGroups];  // uint8 {128 B, M, K/256}, box {128, 128, BK/256}, 128B swizzle
@@ -96,6 +101,7 @@ struct GemmConfig {
     // drain at the end waits on it)
     static_assert(STAGES_ % PRODUCERS_ == 0, "stages must be a multiple of the producer pairs");
     static constexpr int kThreads = 32 * (kFirstProducerWarp + 2 * kProducers);
+    static_assert(kThreads <= 1024, "too many warps");
     static constexpr int kEpiCols = EPI_COLS_;
     static constexpr int kEpiBufs = EPI_BUFS_;
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
@@ -114,8 +120,8 @@ struct GemmConfig {
     static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;  // 32 rows of one chunk
     static constexpr int kEpiOff = kStages * kStageBytes;
     static constexpr int kBarOff = kEpiOff + 4 * kEpiBufs * kEpiBufBytes;
-    // full[S], empty[S], acc_full[2], acc_empty[2], drain
-    static constexpr int kNumBars = 2 * kStages + 5;
+    // full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain, sf_drain
+    static constexpr int kNumBars = 3 * kStages + 6;
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
@@ -369,9 +375,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t bar0 = base + Cfg::kBarOff;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+    const uint32_t sf_drain_bar = bar0 + 8u * (3 * S + 5);
     const uint32_t tmem_slot = base + Cfg::kSlotOff;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 4);
 
@@ -382,12 +390,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full_bar(s), 2);   // one A and one B producer per stage
             ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(sfr_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
             ptx::mbar_init(acce_bar(b), 4);  // lane 0 of each epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(sf_drain_bar, 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -412,11 +422,54 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             else
                 producer_role<Cfg, false>(p, base, bar0, wctx, pw >> 1);
         }
+    } else if (warp == kSfWarp) {
+        if (lane == 0) {
+            // ------------------------------------------- scale copies
+            // once a stage's data has landed, copy its scale atoms into the
+            // slot's own tensor-memory columns and signal sf_ready[slot]; the
+            // MMA thread waits on that instead of full[slot]
+            uint32_t q = 0;
+            bool ok = true, issued_any = false;
+            int g = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileCoord tc = tile_coord(p, t, g);
+                const int kchunks = p.kchunks[tc.g];
+                const int nst = stages_of<Cfg::BK>(kchunks);
+                for (int it = 0; it < nst; ++it, ++q) {
+                    const int stage = (int)(q % S);
+                    if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
+                    const uint32_t ssfa = base + stage * Cfg::kStageBytes + Cfg::kABytes + Cfg::kBBytes;
+                    const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+#pragma unroll
+                    for (int j = 0; j < Cfg::kMmas; ++j) {
+                        if (j < nk) {
+                            ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::sfa_col(stage, j),
+                                                      desc_scale_atom(ssfa + 512 * j));
+#pragma unroll
+                            for (int h = 0; h < BN / 128; ++h)
+                                ptx::tc_cp_32x128b_warpx4(
+                                    tmem_base + Cfg::sfb_col(stage, j, h),
+                                    desc_scale_atom(ssfb + Cfg::kMmas * 512 * h + 512 * j));
+                        }
+                    }
+                    ptx::tc_commit(sfr_bar(stage));
+                    issued_any = true;
+                }
+            }
+            if (issued_any) {   // copies in flight write tensor memory: wait for them
+                ptx::tc_commit(sf_drain_bar);
+                wait_drain(sf_drain_bar, 0u, wctx);
+            }
+        }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            int stage = 0;
-            uint32_t phase = 0;
+            uint32_t q = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
@@ -431,8 +484,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int it = 0; it < nst; ++it) {
-                    if (!wait_bounded(full_bar(stage), phase, wctx, kRoleMma)) {
+                for (int it = 0; it < nst; ++it, ++q) {
+                    const int stage = (int)(q % S);
+                    // sf_ready implies full: the scale thread waited for it
+                    if (!wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
                         ok = false;
                         break;
                     }
@@ -440,20 +495,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
                     const uint32_t sa = base + stage * Cfg::kStageBytes;
                     const uint32_t sb = sa + Cfg::kABytes;
-                    const uint32_t ssfa = sb + Cfg::kBBytes;
-                    const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
-#pragma unroll
-                    for (int j = 0; j < Cfg::kMmas; ++j) {
-                        if (j < nk) {
-                            ptx::tc_cp_32x128b_warpx4(tmem_base + Cfg::sfa_col(stage, j),
-                                                      desc_scale_atom(ssfa + 512 * j));
-#pragma unroll
-                            for (int h = 0; h < BN / 128; ++h)
-                                ptx::tc_cp_32x128b_warpx4(
-                                    tmem_base + Cfg::sfb_col(stage, j, h),
-                                    desc_scale_atom(ssfb + Cfg::kMmas * 512 * h + 512 * j));
-                        }
-                    }
 #pragma unroll
                     for (int j = 0; j < Cfg::kMmas; ++j) {
                         if (j < nk) {
@@ -467,12 +508,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                               (it > 0 || j > 0) ? 1u : 0u);
                         }
                     }
+                    // frees the slot once these MMAs (and, through sf_ready,
+                    // the scale copies before them) are complete
                     ptx::tc_commit(empty_bar(stage));
                     issued_any = true;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
                 if (!ok)
                     break;
