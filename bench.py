@@ -142,12 +142,8 @@ def dist_env():
 
 
 def max_over_ranks(x: float, ws: int) -> float:
-    if ws == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from block_scaled_nvfp4_group_gb300 import shard
+    return shard.max_over_ranks(x, device="cuda") if ws > 1 else x
 
 
 def barrier(ws: int):
@@ -248,8 +244,10 @@ def run_ours(args):
 
     wl = workloads.make_workload(args.workload)
     if rank > 0:    # every rank its own batch of the same shapes
+        from block_scaled_nvfp4_group_gb300 import shard
         wl = workloads.Workload(wl.name, wl.seed,
-                                workloads.make_groups(wl.shapes(), wl.seed + 7919 + 1000 * rank))
+                                workloads.make_groups(wl.shapes(),
+                                                      shard.rank_seed(wl.seed + 7919, rank)))
     shapes = wl.shapes()
     flops = flops_of(shapes)
     gemm_bytes = bytes_of(shapes)
@@ -408,7 +406,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="moe_gate_up")

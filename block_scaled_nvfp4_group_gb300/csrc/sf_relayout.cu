@@ -9,10 +9,10 @@
 // the 32 x 16-byte shape of one tcgen05.cp 32x128b.warpx4 (474067,
 // tcgen05_cp_nvfp4).  Rows past `rows` in the last block become zero.
 //
-// The relayout is a byte permutation, HBM-bound: one CTA moves a
-// 128-row x 64-scale block (8 KiB in, 8 KiB out) through shared memory, with
-// 16-byte loads along source rows and 16-byte stores along atom rows, both
-// coalesced.  Algorithmic traffic: rows * K/16 bytes read, the tiled size
+// The relayout is a byte permutation, HBM-bound: one CTA moves up to four
+// 128-row x 64-scale blocks (32 KiB in, 32 KiB out) through shared memory,
+// with 16-byte loads along source rows (all issued before the first wait) and
+// 16-byte stores along atom rows, both coalesced.  Algorithmic traffic: rows * K/16 bytes read, the tiled size
 // written.
 #include <cuda_runtime.h>
 
@@ -26,10 +26,13 @@ namespace {
 
 constexpr int kMaxDescs = 64;     // relayouts per launch (param block)
 constexpr int kChunkScales = 64;  // scale columns per CTA = 16 atoms
+constexpr int kRowBlocks = 4;     // 128-row blocks per CTA
 constexpr int kThreads = 256;
 constexpr int kPitchWords = 17;   // 64 bytes + 4 bytes pad per staged row
 constexpr int kMaxDim = 1 << 20;
 constexpr int kMaxCount = 4096;
+// 16-byte loads per thread: kRowBlocks * 128 rows * 4 vectors / kThreads
+constexpr int kLoadsPerThread = kRowBlocks * 128 * (kChunkScales / 16) / kThreads;
 
 struct RelayoutParams {
     const uint8_t *src[kMaxDescs];
@@ -37,13 +40,16 @@ struct RelayoutParams {
     int rows[kMaxDescs];
     int kcols[kMaxDescs];     // K / 16 scale columns per row
     int chunks[kMaxDescs];    // ceil(kcols / 64)
-    int item_end[kMaxDescs];  // inclusive prefix sum of row blocks * chunks
+    int item_end[kMaxDescs];  // inclusive prefix sum of row-block groups * chunks
     int count;
 };
 
+// One CTA: kRowBlocks consecutive 128-row blocks x one 64-column chunk.
+// Every thread issues all of its 16-byte loads before the first shared store,
+// so a CTA keeps up to 32 KiB of reads in flight.
 __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
 {
-    __shared__ uint32_t tile[128 * kPitchWords];
+    __shared__ uint32_t tile[kRowBlocks * 128 * kPitchWords];
 
     const int item = blockIdx.x;
     int d = 0;
@@ -51,40 +57,57 @@ __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_cons
         ++d;
     const int local = item - (d > 0 ? p.item_end[d - 1] : 0);
     const int chunks = p.chunks[d];
-    const int rb = local / chunks;
+    const int rbg = local / chunks;             // group of kRowBlocks row blocks
     const int kc = local % chunks;
     const int kcols = p.kcols[d];
     const int rows = p.rows[d];
+    const int rblocks = (rows + 127) / 128;
+    const int nrb = min(kRowBlocks, rblocks - rbg * kRowBlocks);   // row blocks here
     const int width = min(kChunkScales, kcols - kc * kChunkScales);  // multiple of 16
     const int nvec = width / 16;
+    const int row0 = rbg * kRowBlocks * 128;
 
-    // stage 128 rows x `width` scale bytes, zero past the last row
+    // loads: rows [row0, row0 + nrb*128) x `width` bytes, zero past `rows`
     const uint8_t *src = p.src[d] + (size_t)kc * kChunkScales;
-    for (int v = threadIdx.x; v < 128 * nvec; v += kThreads) {
+    const int nload = nrb * 128 * nvec;
+    uint4 x[kLoadsPerThread];
+#pragma unroll
+    for (int i = 0; i < kLoadsPerThread; ++i) {
+        const int v = threadIdx.x + i * kThreads;
         const int r = v / nvec, c = v % nvec;
-        const int grow = rb * 128 + r;
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (grow < rows)
-            x = __ldcs(reinterpret_cast<const uint4 *>(src + (size_t)grow * kcols) + c);
-        uint32_t *t = tile + r * kPitchWords + c * 4;
-        t[0] = x.x;
-        t[1] = x.y;
-        t[2] = x.z;
-        t[3] = x.w;
+        x[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (v < nload && row0 + r < rows)
+            x[i] = __ldcs(reinterpret_cast<const uint4 *>(src + (size_t)(row0 + r) * kcols) + c);
+    }
+#pragma unroll
+    for (int i = 0; i < kLoadsPerThread; ++i) {
+        const int v = threadIdx.x + i * kThreads;
+        if (v < nload) {
+            const int r = v / nvec, c = v % nvec;
+            uint32_t *t = tile + r * kPitchWords + c * 4;
+            t[0] = x[i].x;
+            t[1] = x[i].y;
+            t[2] = x[i].z;
+            t[3] = x[i].w;
+        }
     }
     __syncthreads();
 
-    // atom a of this chunk: 16-byte row q holds rows q, q+32, q+64, q+96
+    // atom a of row block rr: 16-byte row q holds rows q, q+32, q+64, q+96
     const int natoms = width / 4;
-    uint8_t *dst = p.dst[d] + ((size_t)rb * (kcols / 4) + (size_t)kc * (kChunkScales / 4)) * 512;
-    for (int o = threadIdx.x; o < natoms * 32; o += kThreads) {
-        const int a = o >> 5, q = o & 31;
+    const int nout = nrb * natoms * 32;
+    for (int o = threadIdx.x; o < nout; o += kThreads) {
+        const int rr = o / (natoms * 32);
+        const int a = (o >> 5) % natoms, q = o & 31;
+        const uint32_t *t = tile + rr * 128 * kPitchWords;
         uint4 y;
-        y.x = tile[(q)*kPitchWords + a];
-        y.y = tile[(q + 32) * kPitchWords + a];
-        y.z = tile[(q + 64) * kPitchWords + a];
-        y.w = tile[(q + 96) * kPitchWords + a];
-        *reinterpret_cast<uint4 *>(dst + (size_t)a * 512 + q * 16) = y;
+        y.x = t[(q)*kPitchWords + a];
+        y.y = t[(q + 32) * kPitchWords + a];
+        y.z = t[(q + 64) * kPitchWords + a];
+        y.w = t[(q + 96) * kPitchWords + a];
+        const size_t rb = (size_t)rbg * kRowBlocks + rr;
+        uint8_t *dst = p.dst[d] + (rb * (kcols / 4) + (size_t)kc * (kChunkScales / 4) + a) * 512;
+        *reinterpret_cast<uint4 *>(dst + q * 16) = y;
     }
 }
 
@@ -145,7 +168,8 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
             continue;
         const int kcols = d.K / 16;
         const int chunks = (kcols + kChunkScales - 1) / kChunkScales;
-        const long long n = (long long)((d.rows + 127) / 128) * chunks;
+        const int rblocks = (d.rows + 127) / 128;
+        const long long n = (long long)((rblocks + kRowBlocks - 1) / kRowBlocks) * chunks;
         if (P.count == kMaxDescs || (long long)items + n > (1ll << 30)) {
             rc = launch();
             if (rc != NVFP4_OK)
