@@ -15,6 +15,8 @@
 //              pairs take the stages round robin: on GB300 the TMA operations
 //              of one issuing thread complete roughly one after another, so
 //              several issuing warps keep more loads in flight;
+//   last warp  L2 prefetcher (optional): B tiles and scales of the stages up
+//              to `pf_stages` ahead of the MMAs, beyond what the ring holds;
 //   warp 5     scale copier (one thread): once a stage has landed,
 //              tcgen05.cp of its scale atoms into the slot's own
 //              tensor-memory columns, then tcgen05.commit to sf_ready[slot]
@@ -100,7 +102,8 @@ struct GemmConfig {
     // that a producer's last issue of a slot is that slot's last phase (the
     // drain at the end waits on it)
     static_assert(STAGES_ % PRODUCERS_ == 0, "stages must be a multiple of the producer pairs");
-    static constexpr int kThreads = 32 * (kFirstProducerWarp + 2 * kProducers);
+    static constexpr int kPrefetchWarp = kFirstProducerWarp + 2 * kProducers;
+    static constexpr int kThreads = 32 * (kPrefetchWarp + 1);
     static_assert(kThreads <= 1024, "too many warps");
     static constexpr int kEpiCols = EPI_COLS_;
     static constexpr int kEpiBufs = EPI_BUFS_;
@@ -122,7 +125,7 @@ struct GemmConfig {
     static constexpr int kBarOff = kEpiOff + 4 * kEpiBufs * kEpiBufBytes;
     // full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain, sf_drain
     static constexpr int kNumBars = 3 * kStages + 6;
-    static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
+    static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag, MMA progress
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
     // tensor memory: accumulators, then one scale region per ring slot
@@ -299,12 +302,6 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
                                  : p.b_policy == 2 ? ptx::policy_evict_last()
                                                    : ptx::policy_evict_normal())
                               : ptx::policy_evict_last();
-    StageCursor<Cfg::BK> pf;   // only the first B producer prefetches
-    pf.start(p, (IS_B && cls == 0) ? (int)blockIdx.x : p.total_tiles);
-    for (int i = 0; i < p.pf_stages && pf.valid(p); ++i) {  // run pf_stages ahead of the loads
-        ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks, pol);
-        pf.advance(p);
-    }
     uint32_t q = 0;   // position in this CTA's sequence of stages
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
@@ -342,11 +339,6 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
-            for (int i = 0; i < Cfg::kProducers && pf.valid(p); ++i) {
-                ptx::tma_prefetch_3d(&p.tmB[pf.tc.g], 0, pf.tc.bn * Cfg::BN, pf.it * Cfg::kChunks,
-                                     pol);
-                pf.advance(p);
-            }
         }
     }
     // copies issued but never consumed (after an abort anywhere in the CTA)
@@ -357,6 +349,44 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
     for (int s = 0; s < S; ++s)
         if (issued & (1u << s))
             wait_drain(full_bar(s), (issued_parity >> s) & 1u, wctx);
+}
+
+// L2 prefetch role (one thread): walks this CTA's stage sequence and
+// prefetches each stage's B tile and B scales into L2 once the MMA thread is
+// within `pf_stages` stages of it, so that more HBM reads are in flight than
+// the shared-memory ring holds.  It only ever delays itself: it gives up
+// (without an error) when a wait for progress exceeds the wait timeout or
+// another role aborted.
+template <class Cfg>
+__device__ __forceinline__ void prefetch_role(const GemmParams &p, volatile uint32_t *progress,
+                                              const WaitCtx &wctx)
+{
+    const uint64_t pol = p.b_policy == 1   ? ptx::policy_evict_first()
+                         : p.b_policy == 2 ? ptx::policy_evict_last()
+                                           : ptx::policy_evict_normal();
+    StageCursor<Cfg::BK> c;
+    c.start(p, blockIdx.x);
+    uint32_t q = 0;
+    while (c.valid(p)) {
+        if (q >= *progress + (uint32_t)p.pf_stages) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (q >= *progress + (uint32_t)p.pf_stages) {
+                if (*wctx.abort || ptx::globaltimer_ns() - t0 > wctx.timeout_ns)
+                    return;
+                __nanosleep(128);
+            }
+        }
+        const int kblk = p.kchunks[c.tc.g] * (kChunkK / kMmaK);
+        const int nk = kblocks_in_stage<Cfg::BK>(p.kchunks[c.tc.g], c.it);
+        ptx::tma_prefetch_3d(&p.tmB[c.tc.g], 0, c.tc.bn * Cfg::BN, c.it * Cfg::kChunks, pol);
+#pragma unroll
+        for (int h = 0; h < Cfg::BN / 128; ++h)
+            ptx::bulk_prefetch(p.sfb[c.tc.g] + ((size_t)(c.tc.bn * (Cfg::BN / 128) + h) * kblk +
+                                                (size_t)c.it * Cfg::kMmas) * 512,
+                               nk * 512, pol);
+        c.advance(p);
+        ++q;
+    }
 }
 
 template <class Cfg>
@@ -382,6 +412,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const uint32_t sf_drain_bar = bar0 + 8u * (3 * S + 5);
     const uint32_t tmem_slot = base + Cfg::kSlotOff;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 4);
+    volatile uint32_t *mma_progress = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -399,6 +430,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(sf_drain_bar, 1);
         *abort_flag = 0u;
+        *mma_progress = 0u;
         ptx::fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -413,7 +445,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};
     const int total = p.total_tiles;
 
-    if (warp >= kFirstProducerWarp) {
+    if (warp == Cfg::kPrefetchWarp) {
+        if (lane == 0 && p.pf_stages > 0)
+            prefetch_role<Cfg>(p, mma_progress, wctx);
+    } else if (warp >= kFirstProducerWarp) {
         // producer warps: A, B, A, B, ... for stage classes 0, 0, 1, 1, ...
         const int pw = warp - kFirstProducerWarp;
         if (lane == 0) {
@@ -512,6 +547,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                     // the scale copies before them) are complete
                     ptx::tc_commit(empty_bar(stage));
                     issued_any = true;
+                    *mma_progress = q + 1;   // paces the L2 prefetcher
                 }
                 if (!ok)
                     break;

@@ -115,6 +115,14 @@ __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, 
         : "memory");
 }
 
+// L2 prefetch of a contiguous range (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_prefetch(const void *src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes),
+                 "l"(policy)
+                 : "memory");
+}
+
 // contiguous bulk load global -> shared (16-byte aligned, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar, uint64_t policy)
