@@ -28,8 +28,9 @@
 //              and tcgen05.commit to free the stage / hand the accumulator on.
 // The ring of STAGES shared-memory slots is guarded by mbarrier full/empty
 // pairs (full counts the A and B producers' arrivals plus the copied bytes).
-// With two accumulators the epilogue of tile t overlaps the MMAs of t+1;
-// with one, the producers still stream tile t+1's stages meanwhile.
+// The epilogue hands the accumulator back as soon as it holds the tile in
+// registers (as FP16), so its stores overlap the MMAs of the next tile; with
+// two accumulators (BN = 128) the MMAs do not even wait for its loads.
 //
 // The warp roles, the scale addressing and the descriptor fields follow
 // kernelbot nvfp4-group-gemm submission 474067 (group_gemm_persistent_kernel,
@@ -587,69 +588,67 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int N = p.N[tc.g];
             const int m0 = tc.bm * kBM + warp * 32;
             const int n0 = tc.bn * BN;
+            // 1. this thread's whole accumulator row -> FP16 pairs in registers
+            uint32_t h[BN / 2];
             if (m0 < M) {
-#pragma unroll 1
-                for (int c = 0; c < BN / EC; ++c) {
-                    if (n0 + c * EC >= N)
-                        break;
-                    uint32_t h[EC / 2];
-                    {
-                        const uint32_t ta = tmem_base + lane_tmem + acc * BN + c * EC;
-                        uint32_t v0[32];
-                        ptx::tmem_ld_32x32b_x32(ta, v0);
-                        if constexpr (EC == 64) {
-                            uint32_t v1[32];
-                            ptx::tmem_ld_32x32b_x32(ta + 32, v1);
-                            ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                h[i] = pack_half2_rn(v0[2 * i], v0[2 * i + 1]);
-                                h[16 + i] = pack_half2_rn(v1[2 * i], v1[2 * i + 1]);
-                            }
-                        } else {
-                            ptx::tmem_wait_ld();
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (n0 + c * 32 < N) {   // warp-uniform
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_tmem + acc * BN + c * 32, v);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                h[i] = pack_half2_rn(v0[2 * i], v0[2 * i + 1]);
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            h[c * 16 + i] = pack_half2_rn(v[2 * i], v[2 * i + 1]);
                     }
-                    // the store that last used this buffer must have finished
-                    // reading it
-                    if (lane == 0) {
-                        if constexpr (Cfg::kEpiBufs == 2)
-                            ptx::bulk_wait_group_read<1>();
-                        else
-                            ptx::bulk_wait_group_read<0>();
-                    }
-                    __syncwarp();
-                    const uint32_t buf = stage_buf + sbuf * Cfg::kEpiBufBytes;
-                    // one row of EC halves per lane; 16-byte chunk q of row r
-                    // sits at chunk q ^ (swizzle phase of r), the pattern of
-                    // the C tensor map's EC*2-byte swizzle (conflict-free)
-                    constexpr int kQ = EC / 8;
-                    const uint32_t row = buf + lane * (EC * 2);
-                    const int phase_r = (EC == 64) ? (lane & 7) : ((lane >> 1) & 3);
-#pragma unroll
-                    for (int q = 0; q < kQ; ++q)
-                        ptx::st_shared_v4(row + ((q ^ phase_r) << 4), h[4 * q], h[4 * q + 1],
-                                          h[4 * q + 2], h[4 * q + 3]);
-                    ptx::fence_proxy_async_shared();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&p.tmC[tc.g], buf, n0 + c * EC, m0);
-                        ptx::bulk_commit_group();
-                    }
-                    __syncwarp();
-                    if constexpr (Cfg::kEpiBufs == 2)
-                        sbuf ^= 1;
                 }
             }
-            // every lane's loads have completed (wait::ld): hand the
-            // accumulator back to the MMA thread
+            // 2. every lane's loads have completed (wait::ld): the accumulator
+            // goes back to the MMA thread before the stores start, so the next
+            // tile's MMAs overlap them
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(acce_bar(acc));
+            // 3. swizzled shared staging + TMA tensor stores, EC columns each
+            if (m0 < M) {
+#pragma unroll
+                for (int c = 0; c < BN / EC; ++c) {
+                    if (n0 + c * EC < N) {   // warp-uniform
+                        // the store that last used this buffer must have
+                        // finished reading it
+                        if (lane == 0) {
+                            if constexpr (Cfg::kEpiBufs == 2)
+                                ptx::bulk_wait_group_read<1>();
+                            else
+                                ptx::bulk_wait_group_read<0>();
+                        }
+                        __syncwarp();
+                        const uint32_t buf = stage_buf + sbuf * Cfg::kEpiBufBytes;
+                        // one row of EC halves per lane; 16-byte chunk q of row
+                        // r sits at chunk q ^ (swizzle phase of r), the pattern
+                        // of the C tensor map's EC*2-byte swizzle
+                        // (conflict-free)
+                        constexpr int kQ = EC / 8;
+                        const uint32_t row = buf + lane * (EC * 2);
+                        const int phase_r = (EC == 64) ? (lane & 7) : ((lane >> 1) & 3);
+#pragma unroll
+                        for (int q = 0; q < kQ; ++q)
+                            ptx::st_shared_v4(row + ((q ^ phase_r) << 4), h[c * (EC / 2) + 4 * q],
+                                              h[c * (EC / 2) + 4 * q + 1], h[c * (EC / 2) + 4 * q + 2],
+                                              h[c * (EC / 2) + 4 * q + 3]);
+                        ptx::fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmC[tc.g], buf, n0 + c * EC, m0);
+                            ptx::bulk_commit_group();
+                        }
+                        __syncwarp();
+                        if constexpr (Cfg::kEpiBufs == 2)
+                            sbuf ^= 1;
+                    }
+                }
+            }
             if (++acc == Cfg::kAccBufs) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -681,11 +680,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 //               per warp (64-column stores)
 // The last parameter is the number of producer pairs.
 // ---------------------------------------------------------------------------
-using CfgStream = GemmConfig<128, 512, 3, 32, 1, 3>;
-using CfgWide = GemmConfig<256, 256, 4, 32, 1, 4>;
-using CfgWide512 = GemmConfig<256, 512, 2, 32, 1, 2>;
-using CfgCompute = GemmConfig<128, 256, 4, 64, 2, 4>;
-using CfgWideP1 = GemmConfig<256, 256, 4, 32, 1, 1>;
+using CfgStream = GemmConfig<128, 512, 3, 32, 1, 1>;
+using CfgWide = GemmConfig<256, 256, 4, 32, 1, 1>;
+using CfgWide512 = GemmConfig<256, 512, 2, 32, 1, 1>;
+using CfgCompute = GemmConfig<128, 256, 4, 64, 2, 1>;
 using CfgWideP2 = GemmConfig<256, 256, 4, 32, 1, 2>;
+using CfgWideP4 = GemmConfig<256, 256, 4, 32, 1, 4>;
 
 }  // namespace nvfp4

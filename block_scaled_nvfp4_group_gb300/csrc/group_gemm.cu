@@ -25,14 +25,14 @@ enum Kind : int {
     kKindWide = 1,
     kKindCompute = 2,
     kKindWide512 = 3,
-    kKindWideP1 = 4,
-    kKindWideP2 = 5,
+    kKindWideP2 = 4,
+    kKindWideP4 = 5,
     kNumKinds = 6
 };
 
 bool needs_n256(int kind)
 {
-    return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP1 || kind == kKindWideP2;
+    return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4;
 }
 
 template <class Cfg>
@@ -61,7 +61,7 @@ const KindInfo &kind_info(int k)
 {
     static const KindInfo table[kNumKinds] = {make_kind<CfgStream>(),  make_kind<CfgWide>(),
                                               make_kind<CfgCompute>(), make_kind<CfgWide512>(),
-                                              make_kind<CfgWideP1>(),  make_kind<CfgWideP2>()};
+                                              make_kind<CfgWideP2>(),  make_kind<CfgWideP4>()};
     return table[k];
 }
 

@@ -44,12 +44,13 @@ class DeviceProblem:
             if M > 0:   # an empty group is skipped by the GEMM as well
                 self.relayout_items.append((self.SFA[i], self.SFA_t[i], M, K))
                 self.relayout_items.append((self.SFB[i], self.SFB_t[i], N, K))
+        self.relayout_descs = ops.make_relayout_descs(self.relayout_items)
         self.descs = ops.make_group_descs(
             (self.A[i], self.B[i], self.SFA_t[i], self.SFB_t[i], self.C[i], M, N, K)
             for i, (M, N, K) in enumerate(self.shapes))
 
     def relayout(self, stream=None) -> None:
-        ops.sf_relayout_group(self.relayout_items, stream=stream)
+        ops.sf_relayout_group(None, stream=stream, descs=self.relayout_descs)
 
     def gemm(self, stream=None) -> None:
         ops.group_gemm(None, stream=stream, descs=self.descs)

@@ -48,9 +48,8 @@ def sf_relayout(sf: torch.Tensor, rows: int, K: int, out: torch.Tensor | None = 
     return out
 
 
-def sf_relayout_group(items, stream=None) -> None:
-    """items: iterable of (src, dst, rows, K) device tensors; one launch."""
-    lib = _abi.load()
+def make_relayout_descs(items):
+    """items: iterable of (src, dst, rows, K) device tensors."""
     items = list(items)
     arr = (_abi.SfRelayoutDesc * len(items))()
     for i, (src, dst, rows, K) in enumerate(items):
@@ -58,7 +57,17 @@ def sf_relayout_group(items, stream=None) -> None:
         if dst.numel() < sf_tiled_bytes(rows, K):
             raise ValueError("dst too small")
         arr[i] = _abi.SfRelayoutDesc(src.data_ptr(), dst.data_ptr(), rows, K)
-    _abi.check(lib.nvfp4_sf_relayout_group(arr, len(items), _stream_handle(stream)),
+    return arr
+
+
+def sf_relayout_group(items, stream=None, descs=None) -> None:
+    """items: iterable of (src, dst, rows, K) device tensors; one launch.
+    `descs` may carry a prebuilt array (make_relayout_descs)."""
+    lib = _abi.load()
+    arr = descs if descs is not None else make_relayout_descs(items)
+    if len(arr) == 0:
+        return
+    _abi.check(lib.nvfp4_sf_relayout_group(arr, len(arr), _stream_handle(stream)),
                "nvfp4_sf_relayout_group")
 
 

@@ -58,7 +58,7 @@ def test_ragged_several_tiles(kind):
         run_and_compare(workloads.make_groups(shapes, seed=2))
 
 
-@pytest.mark.parametrize("kind", ["wide", "wide512", "wide_p1", "wide_p2"])
+@pytest.mark.parametrize("kind", ["wide", "wide512", "wide_p2", "wide_p4"])
 def test_wide_tiles_ragged_m(kind):
     """BN = 256 tiles (two scale blocks per B tile), ragged M, several N
     tiles, one- and multi-stage K, half last stages."""
