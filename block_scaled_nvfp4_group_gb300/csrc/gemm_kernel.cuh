@@ -442,6 +442,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = ptx::ld_shared_u32(tmem_slot);
+    // With a programmatic launch the set-up above overlaps the previous
+    // kernel; nothing below touches global memory before that kernel is done.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};
     const int total = p.total_tiles;

@@ -35,10 +35,23 @@ bool needs_n256(int kind)
     return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4;
 }
 
+// Launch with programmatic stream serialization (unless NVFP4_PDL=0): the
+// kernel may start while the previous kernel in the stream finishes, and
+// waits for it (griddepcontrol.wait) before touching global memory.
 template <class Cfg>
-void launch_kind(const GemmParams &P, int grid, cudaStream_t s)
+cudaError_t launch_kind(const GemmParams &P, int grid, cudaStream_t s)
 {
-    nvfp4_group_gemm_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(P);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = env_int("NVFP4_PDL", 1) != 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, nvfp4_group_gemm_kernel<Cfg>, P);
 }
 
 struct KindInfo {
@@ -47,7 +60,7 @@ struct KindInfo {
     int epi_cols;
     int smem;
     const void *fn;
-    void (*launch)(const GemmParams &, int, cudaStream_t);
+    cudaError_t (*launch)(const GemmParams &, int, cudaStream_t);
 };
 
 template <class Cfg>
@@ -226,8 +239,7 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
     for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
         const GemmParams &P = plist[l];
         const int grid = P.total_tiles < sm_count ? P.total_tiles : sm_count;
-        ki.launch(P, grid, stream);
-        if (cudaGetLastError() != cudaSuccess)
+        if (ki.launch(P, grid, stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
             rc = NVFP4_ERR_CUDA;
     }
     return rc;

@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "../../include/nvfp4_group_gemm.h"
+#include "ptx.cuh"
 #include "runtime.h"
 
 namespace nvfp4 {
@@ -50,6 +51,10 @@ struct RelayoutParams {
 __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
 {
     __shared__ uint32_t tile[kRowBlocks * 128 * kPitchWords];
+    // programmatic launch: start early, but read and write global memory only
+    // once the previous kernel in the stream is done
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     const int item = blockIdx.x;
     int d = 0;
@@ -157,7 +162,18 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
     auto launch = [&]() -> int {
         if (P.count == 0)
             return NVFP4_OK;
-        sf_relayout_kernel<<<P.item_end[P.count - 1], kThreads, 0, stream>>>(P);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(P.item_end[P.count - 1]);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = env_int("NVFP4_PDL", 1) != 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, sf_relayout_kernel, P) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
     };
     P.count = 0;
