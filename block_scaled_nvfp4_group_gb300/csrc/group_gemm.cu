@@ -152,11 +152,12 @@ int choose_b_policy()
     return (o >= 0 && o <= 2) ? o : 0;
 }
 
-// L2 prefetch distance (stages ahead of the ring) for B; off unless asked
+// L2 prefetch distance for B, in stages ahead of the MMAs: 6 measured best
+// on the MoE shapes (the ring holds 4 stages); 0 turns the prefetcher off
 int choose_prefetch()
 {
     const int forced = env_int("NVFP4_PF_STAGES", -1);
-    return forced >= 0 ? forced : 0;
+    return forced >= 0 ? forced : 6;
 }
 
 // launches a call needs for tile width bn (one per 32 non-empty groups,
