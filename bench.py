@@ -37,13 +37,21 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio, GB300
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch from one ncu
 # capture, keyed by workload, valid only for the kernel source it was taken
-# on (sha256 prefix of csrc/gemm_kernel.cuh).  Filled from profiles/.
-NCU_TRAFFIC = {}
+# on (sha256 prefix over the GEMM's source files).  From profiles/.
+NCU_TRAFFIC = {
+    "moe_gate_up": {"bytes": 140443904 + 8526336, "kernel_sha": "4e16f0aa94323990",
+                    "source": "profiles/gemm_moe_gate_up.md"},
+    "square": {"bytes": 75565568 + 92595968, "kernel_sha": "4e16f0aa94323990",
+               "source": "profiles/gemm_square.md"},
+}
+KERNEL_SOURCES = ("gemm_kernel.cuh", "group_gemm.cu", "ptx.cuh")
 
 
 def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "block_scaled_nvfp4_group_gb300", "csrc", "gemm_kernel.cuh")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "block_scaled_nvfp4_group_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks() -> dict:
