@@ -44,7 +44,7 @@ NCU_TRAFFIC = {
     "square": {"bytes": 75565568 + 92595968, "kernel_sha": "4e16f0aa94323990",
                "source": "profiles/gemm_square.md"},
 }
-KERNEL_SOURCES = ("gemm_kernel.cuh", "group_gemm.cu", "ptx.cuh")
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "group_gemm.cu", "ptx.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -263,7 +263,10 @@ def run_ours(args):
     prob = DeviceProblem(wl.groups, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 + (len([s for s in shapes if s[0] > 0]) + 31) // 32
+    from block_scaled_nvfp4_group_gb300 import _abi, ops
+    gemm_kind, gemm_launches = ops.group_gemm_plan(descs=prob.descs)
+    gemm_kernel = _abi.KIND_KERNELS[[k for k, v in _abi.KIND_NAMES.items() if v == gemm_kind][0]]
+    launches_per_step = 1 + gemm_launches
 
     # warm-up (also JIT/driver first-use costs and the library's one-time
     # per-device set-up, which must precede graph capture)
@@ -398,7 +401,7 @@ def run_ours(args):
         "launch": "each step replayed as a captured CUDA graph (relayout + GEMM launches)",
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "nvfp4_group_gemm_kernel",
+                     "kernel": gemm_kernel, "kernel_config": gemm_kind,
                      "peak_source": peaks["source"] + (
                          " (hbm_gbs)" if bound == "hbm" else
                          " (bf16_tflops x 6, nominal fp4/bf16 dense ratio)"),

@@ -20,6 +20,12 @@ NVFP4_ERR_CUDA = -4
 NVFP4_ERR_TIMEOUT = -5
 NVFP4_ERR_TOO_MANY = -6
 
+# kernel configurations (NVFP4_KIND_* in the header) and their kernels
+KIND_NAMES = {0: "stream", 1: "wide", 2: "compute", 3: "wide512", 4: "wide_p2", 5: "wide_p4",
+              6: "pair"}
+KIND_KERNELS = {k: ("nvfp4_group_gemm_pair_kernel" if k == 6 else "nvfp4_group_gemm_kernel")
+                for k in KIND_NAMES}
+
 
 class GroupDesc(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("SFA", ctypes.c_void_p),
@@ -37,6 +43,9 @@ SIGNATURES = {
     "nvfp4_group_gemm": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int, ctypes.c_void_p]),
     "nvfp4_group_gemm_noalloc": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
                                                 ctypes.c_void_p]),
+    "nvfp4_group_gemm_plan": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_int)]),
     "nvfp4_sf_relayout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_void_p]),
     "nvfp4_sf_relayout_group": (ctypes.c_int, [ctypes.POINTER(SfRelayoutDesc), ctypes.c_int,

@@ -9,7 +9,7 @@
 #include <vector>
 
 #include "../../include/nvfp4_group_gemm.h"
-#include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 #include "runtime.h"
 
 namespace nvfp4 {
@@ -20,14 +20,16 @@ constexpr int kMaxGroupsPerCall = 4096;
 constexpr long long kMaxTilesPerLaunch = 1ll << 30;
 constexpr int kMaxDevices = 64;
 
+// kernel configurations: the NVFP4_KIND_* numbers of the C ABI
 enum Kind : int {
-    kKindStream = 0,
-    kKindWide = 1,
-    kKindCompute = 2,
-    kKindWide512 = 3,
-    kKindWideP2 = 4,
-    kKindWideP4 = 5,
-    kNumKinds = 6
+    kKindStream = NVFP4_KIND_STREAM,
+    kKindWide = NVFP4_KIND_WIDE,
+    kKindCompute = NVFP4_KIND_COMPUTE,
+    kKindWide512 = NVFP4_KIND_WIDE512,
+    kKindWideP2 = NVFP4_KIND_WIDE_P2,
+    kKindWideP4 = NVFP4_KIND_WIDE_P4,
+    kKindPair = NVFP4_KIND_PAIR,
+    kNumKinds = 7
 };
 
 bool needs_n256(int kind)
@@ -35,52 +37,94 @@ bool needs_n256(int kind)
     return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4;
 }
 
-// Launch with programmatic stream serialization (unless NVFP4_PDL=0): the
-// kernel may start while the previous kernel in the stream finishes, and
-// waits for it (griddepcontrol.wait) before touching global memory.
-template <class Cfg>
-cudaError_t launch_kind(const GemmParams &P, int grid, cudaStream_t s)
+// Launch configuration shared by every kind: programmatic stream
+// serialization (unless NVFP4_PDL=0), so the kernel may start while the
+// previous kernel in the stream finishes and waits for it
+// (griddepcontrol.wait) before touching global memory; CTA pairs also get a
+// cluster of two.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+};
+
+void make_launch_cfg(LaunchCfg &L, int grid, int threads, int smem, bool pair, cudaStream_t s)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(Cfg::kThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = env_int("NVFP4_PDL", 1) != 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, nvfp4_group_gemm_kernel<Cfg>, P);
+    L.cfg = cudaLaunchConfig_t{};
+    L.cfg.gridDim = dim3(grid);
+    L.cfg.blockDim = dim3(threads);
+    L.cfg.dynamicSmemBytes = smem;
+    L.cfg.stream = s;
+    L.attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    L.attr[0].val.programmaticStreamSerializationAllowed = env_int("NVFP4_PDL", 1) != 0;
+    L.attr[1].id = cudaLaunchAttributeClusterDimension;
+    L.attr[1].val.clusterDim.x = 2;
+    L.attr[1].val.clusterDim.y = 1;
+    L.attr[1].val.clusterDim.z = 1;
+    L.cfg.attrs = L.attr;
+    L.cfg.numAttrs = pair ? 2 : 1;
+}
+
+template <class Cfg>
+cudaError_t launch_kind(const PairParams &P, int grid, cudaStream_t s)
+{
+    LaunchCfg L;
+    make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, false, s);
+    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg>, P.g);
+}
+
+template <class Cfg>
+cudaError_t launch_pair_kind(const PairParams &P, int grid, cudaStream_t s)
+{
+    LaunchCfg L;
+    make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, true, s);
+    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_pair_kernel<Cfg>, P);
 }
 
 struct KindInfo {
+    int bm;         // output rows per tile (256 for CTA pairs)
     int bn;
+    int box_b;      // rows of B one CTA loads per stage
     int chunks;     // 128-byte K chunks per row per stage
     int epi_cols;
+    int threads;
     int smem;
+    bool pair;
     const void *fn;
-    cudaError_t (*launch)(const GemmParams &, int, cudaStream_t);
+    cudaError_t (*launch)(const PairParams &, int, cudaStream_t);
 };
 
 template <class Cfg>
 KindInfo make_kind()
 {
-    return KindInfo{Cfg::BN, Cfg::kChunks, Cfg::kEpiCols, Cfg::kSmemBytes,
+    return KindInfo{kBM, Cfg::BN, Cfg::BN, Cfg::kChunks, Cfg::kEpiCols, Cfg::kThreads,
+                    Cfg::kSmemBytes, false,
                     reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg>), &launch_kind<Cfg>};
+}
+
+template <class Cfg>
+KindInfo make_pair_kind()
+{
+    return KindInfo{Cfg::kPairBM, Cfg::BN, Cfg::BN / 2, 1, Cfg::kEpiCols, Cfg::kThreads,
+                    Cfg::kSmemBytes, true,
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg>),
+                    &launch_pair_kind<Cfg>};
 }
 
 const KindInfo &kind_info(int k)
 {
-    static const KindInfo table[kNumKinds] = {make_kind<CfgStream>(),  make_kind<CfgWide>(),
-                                              make_kind<CfgCompute>(), make_kind<CfgWide512>(),
-                                              make_kind<CfgWideP2>(),  make_kind<CfgWideP4>()};
+    static const KindInfo table[kNumKinds] = {
+        make_kind<CfgStream>(),  make_kind<CfgWide>(),  make_kind<CfgCompute>(),
+        make_kind<CfgWide512>(), make_kind<CfgWideP2>(), make_kind<CfgWideP4>(),
+        make_pair_kind<CfgPair>()};
     return table[k];
 }
 
 std::mutex g_attr_mu;
 bool g_attr_set[kMaxDevices][kNumKinds];
+int g_max_pairs[kMaxDevices][kNumKinds];
 
+// Shared-memory attribute of the kind's kernel on this device and, for CTA
+// pairs, how many pairs can be resident at once (the persistent grid size)
 int ensure_kernel_attributes(int dev, int kind)
 {
     std::lock_guard<std::mutex> lk(g_attr_mu);
@@ -91,9 +135,28 @@ int ensure_kernel_attributes(int dev, int kind)
         if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) !=
             cudaSuccess)
             return NVFP4_ERR_CUDA;
+        if (ki.pair) {
+            LaunchCfg L;
+            make_launch_cfg(L, 2, ki.threads, ki.smem, true, nullptr);
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, ki.fn, &L.cfg) != cudaSuccess ||
+                clusters < 1)
+                return NVFP4_ERR_UNSUPPORTED;
+            g_max_pairs[dev][kind] = clusters;
+        }
         g_attr_set[dev][kind] = true;
     }
     return NVFP4_OK;
+}
+
+// persistent grid of a launch with `tiles` tiles
+int grid_size(int dev, int kind, int tiles, int sm_count)
+{
+    if (kind_info(kind).pair) {
+        const int pairs = g_max_pairs[dev][kind];
+        return 2 * (tiles < pairs ? tiles : pairs);
+    }
+    return tiles < sm_count ? tiles : sm_count;
 }
 
 int validate_group(const GroupDesc &g)
@@ -130,16 +193,38 @@ int validate_call(const GroupDesc *groups, int num_groups)
 // re-reads and the TMA operations per output byte, which the measurements on
 // GB300 show matters for every shape here; they need every N to be a multiple
 // of 256 (a B tile takes two whole 128-row scale blocks).  Otherwise BN = 128
-// with 512-K stages (CfgStream).  NVFP4_GEMM_KIND overrides the choice.
-int choose_kind(const GroupDesc *groups, int n)
+// with 512-K stages (CfgStream).  CTA pairs (CfgPair, 256 x 256 tiles) run a
+// 256 x 256 tile in about 0.92 of the time one CTA takes for a 128 x 256
+// tile, but pad M to 256: they are chosen when the call fills at least four
+// rounds of the grid and pairing does not add a round (large M, e.g. the
+// 4096^3 groups), never for the small-M MoE shapes.  NVFP4_GEMM_KIND
+// overrides the choice.
+int choose_kind(const GroupDesc *groups, int n, int sm_count)
 {
     const int forced = env_int("NVFP4_GEMM_KIND", -1);
-    bool all_n256 = true;
+    bool all_n256 = true, all_n_ge256 = true;
+    long long wide_tiles = 0, pair_tiles = 0;
     for (int i = 0; i < n; ++i)
-        if (groups[i].M > 0)
-            all_n256 = all_n256 && (groups[i].N % 256 == 0);
-    if (forced >= 0 && forced < kNumKinds)
-        return (!needs_n256(forced) || all_n256) ? forced : kKindStream;
+        if (groups[i].M > 0) {
+            const GroupDesc &g = groups[i];
+            all_n256 = all_n256 && (g.N % 256 == 0);
+            all_n_ge256 = all_n_ge256 && (g.N >= 256);
+            wide_tiles += (long long)((g.M + 127) / 128) * ((g.N + 255) / 256);
+            pair_tiles += (long long)((g.M + 255) / 256) * ((g.N + 255) / 256);
+        }
+    if (forced >= 0 && forced < kNumKinds) {
+        if (needs_n256(forced) && !all_n256)
+            return kKindStream;
+        // a pair's B scale load spans two 128-row blocks: N >= 256
+        if (forced == kKindPair && !all_n_ge256)
+            return kKindStream;
+        return forced;
+    }
+    const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+    const long long rounds_wide = (wide_tiles + sm_count - 1) / (sm_count > 0 ? sm_count : 1);
+    const long long rounds_pair = (pair_tiles + pairs - 1) / pairs;
+    if (all_n_ge256 && rounds_wide >= 4 && rounds_pair <= rounds_wide)
+        return kKindPair;
     return all_n256 ? kKindWide : kKindStream;
 }
 
@@ -162,7 +247,7 @@ int choose_prefetch()
 
 // launches a call needs for tile width bn (one per 32 non-empty groups,
 // more only past 2^30 tiles); must agree with plan_and_launch
-int count_launches(const GroupDesc *groups, int num_groups, int bn)
+int count_launches(const GroupDesc *groups, int num_groups, int bm, int bn)
 {
     int launches = 0, in_launch = 0;
     long long tiles_in_launch = 0;
@@ -171,7 +256,7 @@ int count_launches(const GroupDesc *groups, int num_groups, int bn)
         if (g.M == 0)
             continue;
         const long long tiles =
-            (long long)((g.M + kBM - 1) / kBM) * (long long)((g.N + bn - 1) / bn);
+            (long long)((g.M + bm - 1) / bm) * (long long)((g.N + bn - 1) / bn);
         if (launches == 0 || in_launch == kMaxGroups || tiles_in_launch + tiles > kMaxTilesPerLaunch) {
             ++launches;
             in_launch = 0;
@@ -188,10 +273,10 @@ int count_launches(const GroupDesc *groups, int num_groups, int bn)
 // first launch, so a rejected map launches nothing.  The parameter blocks
 // live in a per-thread vector whose capacity is kept between calls.
 template <class ErrFn>
-int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int sm_count,
-                    int kind, ErrFn err_for_launch)
+int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
+                    int sm_count, int kind, ErrFn err_for_launch)
 {
-    static thread_local std::vector<GemmParams> plist;
+    static thread_local std::vector<PairParams> plist;
     const KindInfo &ki = kind_info(kind);
     const int b_policy = choose_b_policy();
     const int pf = choose_prefetch();
@@ -205,25 +290,31 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         const GroupDesc &g = groups[i];
         if (g.M == 0)
             continue;
-        const int grid_m = (g.M + kBM - 1) / kBM;
+        const int grid_m = (g.M + ki.bm - 1) / ki.bm;
         const int grid_n = (g.N + ki.bn - 1) / ki.bn;
         const long long tiles = (long long)grid_m * grid_n;
-        if (plist.empty() || plist.back().num_groups == kMaxGroups ||
-            plist.back().total_tiles + tiles > kMaxTilesPerLaunch) {
+        if (plist.empty() || plist.back().g.num_groups == kMaxGroups ||
+            plist.back().g.total_tiles + tiles > kMaxTilesPerLaunch) {
             plist.emplace_back();
-            GemmParams &P = plist.back();
-            std::memset(&P, 0, sizeof(P));
+            std::memset(&plist.back(), 0, sizeof(PairParams));
+            GemmParams &P = plist.back().g;
             P.err = err_for_launch((int)plist.size() - 1);
             P.timeout_ns = timeout;
             P.b_policy = b_policy;
             P.pf_stages = pf;
             P.debug_drop_stage = drop;
         }
-        GemmParams &P = plist.back();
+        PairParams &PP = plist.back();
+        GemmParams &P = PP.g;
         const int j = P.num_groups;
         rc = encode_map_operand(&P.tmA[j], g.A, (uint64_t)g.M, (uint64_t)g.K, kBM, ki.chunks);
         if (rc == NVFP4_OK)
-            rc = encode_map_operand(&P.tmB[j], g.B, (uint64_t)g.N, (uint64_t)g.K, ki.bn, ki.chunks);
+            rc = encode_map_operand(&P.tmB[j], g.B, (uint64_t)g.N, (uint64_t)g.K, ki.box_b,
+                                    ki.chunks);
+        if (rc == NVFP4_OK && ki.pair)
+            rc = encode_map_sf(&PP.tmSFA[j], g.SFA, (uint64_t)g.M, (uint64_t)g.K, 1);
+        if (rc == NVFP4_OK && ki.pair)
+            rc = encode_map_sf(&PP.tmSFB[j], g.SFB, (uint64_t)g.N, (uint64_t)g.K, ki.bn / 128);
         if (rc == NVFP4_OK)
             rc = encode_map_2d(&P.tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
                                (uint64_t)g.M, (uint64_t)g.N * 2, ki.epi_cols, 32, c_swizzle);
@@ -238,8 +329,8 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         P.num_groups = j + 1;
     }
     for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
-        const GemmParams &P = plist[l];
-        const int grid = P.total_tiles < sm_count ? P.total_tiles : sm_count;
+        const PairParams &P = plist[l];
+        const int grid = grid_size(dev, kind, P.g.total_tiles, sm_count);
         if (ki.launch(P, grid, stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
             rc = NVFP4_ERR_CUDA;
     }
@@ -255,21 +346,40 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
     int rc = validate_call(groups, num_groups);
     if (rc != NVFP4_OK)
         return rc;
-    const int kind = choose_kind(groups, num_groups);
-    if (count_launches(groups, num_groups, kind_info(kind).bn) == 0)
-        return NVFP4_OK;
     DeviceState *dev = nullptr;
     rc = current_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
+    const int kind = choose_kind(groups, num_groups, dev->sm_count);
+    if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+        return NVFP4_OK;
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     rc = ensure_kernel_attributes(dev_id, kind);
     if (rc != NVFP4_OK)
         return rc;
     uint32_t *err = dev->err;
-    return plan_and_launch(groups, num_groups, stream, dev->sm_count, kind,
+    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; });
+}
+
+extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind,
+                                     int *launches)
+{
+    using namespace nvfp4;
+    if (!kind || !launches)
+        return NVFP4_ERR_INVALID_ARGUMENT;
+    int rc = validate_call(groups, num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    DeviceState *dev = nullptr;
+    rc = current_device(&dev);
+    if (rc != NVFP4_OK)
+        return rc;
+    const int k = choose_kind(groups, num_groups, dev->sm_count);
+    *kind = k;
+    *launches = count_launches(groups, num_groups, kind_info(k).bm, kind_info(k).bn);
+    return NVFP4_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -341,18 +451,17 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
     int rc = validate_call(groups, num_groups);
     if (rc != NVFP4_OK)
         return rc;
-    const int kind = choose_kind(groups, num_groups);
-    // each launch needs its own two status words of the static scratch
-    const int launches = count_launches(groups, num_groups, kind_info(kind).bn);
-    if (launches == 0)
-        return NVFP4_OK;
-    if (launches > kNoAllocMaxLaunches)
-        return NVFP4_ERR_TOO_MANY;   // more than 32 launches' worth (> 1024 non-empty groups)
-
     NoAllocDevice *dev = nullptr;
     rc = noalloc_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
+    const int kind = choose_kind(groups, num_groups, dev->sm_count);
+    // each launch needs its own two status words of the static scratch
+    const int launches = count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn);
+    if (launches == 0)
+        return NVFP4_OK;
+    if (launches > kNoAllocMaxLaunches)
+        return NVFP4_ERR_TOO_MANY;   // more than 32 launches' worth (> 1024 non-empty groups)
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     rc = ensure_kernel_attributes(dev_id, kind);
@@ -363,6 +472,6 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
     if (cudaMemsetAsync(dev->scratch, 0, sizeof(uint32_t) * 2 * launches, stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     uint32_t *scratch = dev->scratch;
-    return plan_and_launch(groups, num_groups, stream, dev->sm_count, kind,
+    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [scratch](int l) { return scratch + 2 * l; });
 }

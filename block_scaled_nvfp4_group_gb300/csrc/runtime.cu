@@ -162,6 +162,14 @@ int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_
     return encode_map(out, key);
 }
 
+int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_blocks)
+{
+    const uint64_t atoms = K / 64;
+    const MapKey key{ptr, 128, atoms, (rows + 127) / 128, 512, atoms * 512, 128, 4, box_blocks, 3,
+                     (int)CU_TENSOR_MAP_DATA_TYPE_UINT32, (int)CU_TENSOR_MAP_SWIZZLE_NONE};
+    return encode_map(out, key);
+}
+
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 int debug_drop_stage() { return g_debug_drop.load(std::memory_order_relaxed); }
 int b_policy_override() { return read_env_int("NVFP4_B_POLICY", -1); }

@@ -34,11 +34,18 @@ int encode_map_2d(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, 
 int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K,
                        uint32_t box_rows, uint32_t box_chunks);
 
+// Tiled scale factors of a [rows][K] operand (ceil(rows/128) row blocks of
+// K/64 atoms of 512 bytes) as a 3-D uint32 tensor {128, K/64, row blocks},
+// box {128, 4, box_blocks}, no swizzle: one load brings the 4 atoms of one
+// 256-K stage for box_blocks consecutive row blocks (zeros past the last).
+int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_blocks);
+
 unsigned long long wait_timeout_ns();
 int debug_drop_stage();
 int b_policy_override();   // -1 = use the built-in choice
 // tuning and debug knobs from the environment, read at every call:
-// NVFP4_GEMM_KIND (0 stream, 1 wide, 2 compute, 3 wide with 256-K stages),
+// NVFP4_GEMM_KIND (0 stream, 1 wide, 2 compute, 3 wide with 512-K stages,
+// 4 / 5 wide with 2 / 4 producer pairs, 6 CTA pairs),
 // NVFP4_PF_STAGES, NVFP4_B_POLICY (0 normal, 1 evict_first, 2 evict_last)
 int env_int(const char *name, int fallback);
 

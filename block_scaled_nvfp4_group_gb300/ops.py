@@ -98,6 +98,17 @@ def group_gemm(groups, stream=None, descs=None) -> None:
     _abi.check(lib.nvfp4_group_gemm(arr, len(arr), _stream_handle(stream)), "nvfp4_group_gemm")
 
 
+def group_gemm_plan(groups=None, descs=None):
+    """(kind name, launches) nvfp4_group_gemm would use for these groups on
+    the current device; nothing is launched."""
+    lib = _abi.load()
+    arr = descs if descs is not None else make_group_descs(groups)
+    kind, launches = ctypes.c_int(-1), ctypes.c_int(0)
+    _abi.check(lib.nvfp4_group_gemm_plan(arr, len(arr), ctypes.byref(kind), ctypes.byref(launches)),
+               "nvfp4_group_gemm_plan")
+    return _abi.KIND_NAMES[kind.value], launches.value
+
+
 def last_device_error(stream=None) -> int:
     return int(_abi.load().nvfp4_last_device_error(_stream_handle(stream)))
 

@@ -77,6 +77,34 @@ typedef struct GroupDesc {
  * Returns NVFP4_OK or a negative code; nothing is launched on error. */
 int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream);
 
+/* Kernel configurations of the grouped GEMM (chosen per call from the
+ * shapes; the environment variable NVFP4_GEMM_KIND forces one):
+ *  STREAM  128 x 128 tiles, 512-K stages (any N)
+ *  WIDE    128 x 256 tiles, 256-K stages (every N a multiple of 256)
+ *  COMPUTE 128 x 128 tiles, 256-K stages, 64-column stores
+ *  WIDE512 128 x 256 tiles, 512-K stages
+ *  WIDE_P2 / WIDE_P4  WIDE with two / four producer pairs
+ *  PAIR    256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; N >= 256):
+ *          chosen for large M, when pairing fills at least four rounds of
+ *          the grid without adding one */
+enum {
+    NVFP4_KIND_STREAM = 0,
+    NVFP4_KIND_WIDE = 1,
+    NVFP4_KIND_COMPUTE = 2,
+    NVFP4_KIND_WIDE512 = 3,
+    NVFP4_KIND_WIDE_P2 = 4,
+    NVFP4_KIND_WIDE_P4 = 5,
+    NVFP4_KIND_PAIR = 6
+};
+
+/* The plan nvfp4_group_gemm would follow for these groups on the current
+ * device, without launching anything: *kind (an NVFP4_KIND_* value) and
+ * *launches (kernel launches of the call; 0 when every group is empty).
+ * Validates like nvfp4_group_gemm; needs the device's SM count, so the
+ * first call on a device does its one-time set-up (see nvfp4_group_gemm).
+ * kind and launches: host pointers, written only on NVFP4_OK. */
+int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind, int *launches);
+
 /* The grouped GEMM of nvfp4_group_gemm for callers that are not allowed to
  * allocate device memory: engines and plugins that receive every byte of
  * device memory from an arena planned ahead and may not allocate while they

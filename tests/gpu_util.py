@@ -35,7 +35,8 @@ def compare_fp16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
                              f"oracle {r[tuple(idx[0])]}")
 
 
-KINDS = {"stream": 0, "wide": 1, "compute": 2, "wide512": 3, "wide_p2": 4, "wide_p4": 5}
+KINDS = {"stream": 0, "wide": 1, "compute": 2, "wide512": 3, "wide_p2": 4, "wide_p4": 5,
+         "pair": 6}
 
 
 class gemm_env:

@@ -5,14 +5,20 @@ hang), report NVFP4_ERR_TIMEOUT through nvfp4_last_device_error, leave the
 context usable, and the next call must be correct."""
 import pytest
 
-from gpu_util import compare_fp16, require_gb300
+from gpu_util import compare_fp16, gemm_env, require_gb300
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
 
 
-def test_expired_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("kind", [None, "pair"])
+def test_expired_wait_reports_timeout_and_context_survives(kind):
     require_gb300()
+    with gemm_env(kind):
+        _expired_wait(kind)
+
+
+def _expired_wait(kind):
     from block_scaled_nvfp4_group_gb300 import _abi, ops, workloads
     from block_scaled_nvfp4_group_gb300.device import DeviceProblem
     groups = workloads.make_groups([(200, 512, 2048), (64, 256, 1024)], seed=41)

@@ -69,7 +69,8 @@ def test_wide_tiles_ragged_m(kind):
 
 
 @pytest.mark.parametrize("kind,pf", [("stream", 0), ("stream", 8), ("stream", 40), ("wide", 0),
-                                     ("wide", 8), ("wide512", 0), ("compute", 0)])
+                                     ("wide", 8), ("wide512", 0), ("compute", 0), ("pair", 0),
+                                     ("pair", 2), ("pair", 12)])
 def test_more_stages_than_ring_and_many_tiles(kind, pf):
     """K large enough to wrap the shared-memory ring several times per tile
     and more tiles than SMs (persistent loop, both accumulator buffers), with
@@ -78,6 +79,18 @@ def test_more_stages_than_ring_and_many_tiles(kind, pf):
     shapes = [(384, 2048, 4096), (256, 4096, 2560)]
     with gemm_env(kind, pf):
         run_and_compare(workloads.make_groups(shapes, seed=3))
+
+
+def test_pair_tiles_ragged():
+    """CTA pairs (256 x 256 tiles): M tails that leave the odd CTA of a pair
+    with no rows (M <= 128 past a 256 boundary), N not a multiple of 256 (the
+    odd CTA's B half partly or wholly past N), an empty group, one- and
+    multi-stage K, more tiles than pairs."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(200, 384, 1024), (77, 256, 512), (0, 256, 256), (1, 264, 256), (300, 520, 768),
+              (513, 1024, 2304), (129, 2048, 256)]
+    with gemm_env("pair"):
+        run_and_compare(workloads.make_groups(shapes, seed=22))
 
 
 def test_more_groups_than_one_launch():
@@ -149,25 +162,46 @@ def test_workload_tiny():
     run_and_compare(workloads.make_workload("tiny").groups)
 
 
-def test_workload_quantized():
+@pytest.mark.parametrize("kind", [None, "wide", "pair"])
+def test_workload_quantized(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
-    run_and_compare(workloads.make_workload("quantized").groups)
+    with gemm_env(kind):
+        run_and_compare(workloads.make_workload("quantized").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute"])
+@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute", "pair"])
 def test_workload_moe_down(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
         run_and_compare(workloads.make_workload("moe_down").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute"])
+@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute", "pair"])
 def test_workload_moe_gate_up(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
         run_and_compare(workloads.make_workload("moe_gate_up").groups)
 
 
-def test_workload_square_sampled_rows():
+@pytest.mark.parametrize("kind", [None, "wide", "pair"])
+def test_workload_square_sampled_rows(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
-    run_and_compare(workloads.make_workload("square").groups, rows_per_group=24, seed=9)
+    with gemm_env(kind):
+        run_and_compare(workloads.make_workload("square").groups, rows_per_group=24, seed=9)
+
+
+def test_plan_picks_pairs_only_for_large_m():
+    """The configuration the library picks per shape class: CTA pairs for
+    the 4096^3 groups, 128 x 256 tiles for the small-M MoE shapes, 128 x 128
+    tiles when some N is not a multiple of 256; one launch per 32 groups."""
+    from block_scaled_nvfp4_group_gb300 import ops, workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+
+    def plan(groups):
+        return ops.group_gemm_plan(descs=DeviceProblem(groups).descs)
+
+    assert plan(workloads.make_workload("square").groups) == ("pair", 1)
+    assert plan(workloads.make_workload("moe_gate_up").groups) == ("wide", 1)
+    assert plan(workloads.make_groups([(300, 264, 256)], seed=1)) == ("stream", 1)
+    shapes = [(64, 256, 256)] * 40
+    assert plan(workloads.make_groups(shapes, seed=1)) == ("wide", 2)
