@@ -7,27 +7,24 @@
 //              FP16 (round to nearest even), a swizzled shared-memory tile
 //              per warp and a TMA tensor store, which writes whole row
 //              segments and clips rows >= M and columns >= N;
-//   warps 6..  producer pairs: per stage of BK K-elements, the B warp of a
-//              pair issues one 3-D TMA load of the B tile [BN rows x BK/2
-//              bytes] (128-byte swizzle, BK/256 chunks of 128 bytes per row)
-//              and bulk copies of the matching tiled B scale atoms, the A warp
-//              the same for the A tile [128 x BK/2 bytes] and its scales.  The
-//              pairs take the stages round robin: on GB300 the TMA operations
-//              of one issuing thread complete roughly one after another, so
-//              several issuing warps keep more loads in flight;
-//   last warp  L2 prefetcher (optional): B tiles and scales of the stages up
+//   warps 6-9  loaders, one TMA thread each, one operation per stage each:
+//              the A tile [128 x BK/2 bytes] and the B tile [BN x BK/2 bytes]
+//              (3-D boxes over 128-byte K chunks, 128-byte swizzle) complete
+//              on full[slot]; the A and B scale atoms of the stage (3-D boxes
+//              over the tiled scales) complete on sf_full[slot].  A thread
+//              issues only a few TMA operations per microsecond on GB300, so
+//              the stage's operations are spread over four threads;
+//   warp 10    L2 prefetcher (optional): B tiles and scales of the stages up
 //              to `pf_stages` ahead of the MMAs, beyond what the ring holds;
-//   warp 5     scale copier (one thread): once a stage has landed,
-//              tcgen05.cp of its scale atoms into the slot's own
-//              tensor-memory columns, then tcgen05.commit to sf_ready[slot]
-//              (copies issued by the MMA thread itself did not overlap the
-//              MMAs on GB300);
-//   warp 4     MMA issuer (one thread): after sf_ready[slot], BK/64
-//              tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
-//              per stage into an FP32 accumulator (two of them when BN=128),
-//              and tcgen05.commit to free the stage / hand the accumulator on.
-// The ring of STAGES shared-memory slots is guarded by mbarrier full/empty
-// pairs (full counts the A and B producers' arrivals plus the copied bytes).
+//   warp 5     scale copier (one thread): once a stage's scales have landed
+//              (sf_full, ahead of the larger operand tiles), tcgen05.cp of its
+//              atoms into the slot's own tensor-memory columns, then
+//              tcgen05.commit to sf_ready[slot];
+//   warp 4     MMA issuer (one thread): after full[slot] and sf_ready[slot],
+//              BK/64 tcgen05.mma.kind::mxf4nvf4.block_scale.block16
+//              (128 x BN x 64) per stage into an FP32 accumulator (two of them
+//              when BN=128), and tcgen05.commit to free the stage / hand the
+//              accumulator on.
 // The epilogue hands the accumulator back as soon as it holds the tile in
 // registers (as FP16), so its stores overlap the MMAs of the next tile; with
 // two accumulators (BN = 128) the MMAs do not even wait for its loads.
@@ -35,12 +32,12 @@
 // The warp roles, the scale addressing and the descriptor fields follow
 // kernelbot nvfp4-group-gemm submission 474067 (group_gemm_persistent_kernel,
 // tcgen05_mma_nvfp4, tcgen05_cp_nvfp4, the TMA producer warp); the split
-// producers, the store path, the bounded waits and the tensor-memory budget
-// are this build's own.
+// loaders, the separate scale barrier, the store path, the bounded waits and
+// the tensor-memory budget are this build's own.
 //
 // Every mbarrier wait is bounded: when it expires the waiting role sets the
 // device error word and a shared abort flag, all roles leave their loops, the
-// producers wait (bounded) for the copies they issued, the MMA thread waits
+// loaders wait (bounded) for the copies they issued, the MMA thread waits
 // for its issued tensor-core work, the epilogue waits for its stores, and the
 // CTA frees its tensor memory and exits.
 #pragma once
@@ -59,7 +56,8 @@ constexpr int kMmaK = 64;          // K elements per tcgen05.mma (FP4)
 constexpr int kMaxGroups = 32;     // groups per launch (param block)
 constexpr int kMmaWarp = 4;        // MMA issuer; also allocates / frees tensor memory
 constexpr int kSfWarp = 5;         // scale copies shared -> tensor memory
-constexpr int kFirstProducerWarp = 6;
+constexpr int kFirstLoaderWarp = 6;  // A, B, A scales, B scales
+constexpr int kLoaderRoles = 4;
 constexpr int kSmemLimit = 232448; // 227 KiB per CTA
 
 // error word bits (device_err[0]); device_err[1] records who expired first
@@ -72,8 +70,6 @@ struct GemmParams {
     CUtensorMap tmA[kMaxGroups];  // uint8 {128 B, M, K/256}, box {128, 128, BK/256}, 128B swizzle
     CUtensorMap tmB[kMaxGroups];  // uint8 {128 B, N, K/256}, box {128, BN, BK/256}
     CUtensorMap tmC[kMaxGroups];  // fp16 [M][N], box EPI_COLS x 32, swizzle = EPI_COLS * 2 B
-    const uint8_t *sfa[kMaxGroups];
-    const uint8_t *sfb[kMaxGroups];
     int M[kMaxGroups];
     int N[kMaxGroups];
     int kchunks[kMaxGroups];   // K / 256
@@ -85,25 +81,28 @@ struct GemmParams {
     unsigned long long timeout_ns;
     int b_policy;              // L2 policy of B / SFB loads: 0 normal, 1 first, 2 last
     int pf_stages;             // L2 prefetch distance for B, in stages ahead of the ring (0 = off)
-    int debug_drop_stage;      // test hook: CTA 0's B producer never issues its first stage
+    int debug_drop_stage;      // test hook: CTA 0's B loader never issues its first stage
+};
+
+// Parameter block of a launch: the GEMM parameters and the 3-D maps of the
+// tiled scales (uint32 {128, K/64, row blocks}: one 512-byte atom per
+// (row block, 64-K block)), whose box covers the atoms of one stage for the
+// row blocks of one tile.
+struct KernelParams {
+    GemmParams g;
+    CUtensorMap tmSFA[kMaxGroups];  // box {128, BK/64, 1}
+    CUtensorMap tmSFB[kMaxGroups];  // box {128, BK/64, BN/128} (BN/2 per CTA of a pair: 128 rows each)
 };
 
 // BN: tile width; BK: K elements per stage (256 or 512); STAGES: ring depth;
 // EPI_COLS: columns per epilogue store (32 or 64); EPI_BUFS: staging
-// buffers per epilogue warp (1 or 2); PRODUCERS: producer pairs (one A and
-// one B warp each) taking the stages round robin
-template <int BN_, int BK_, int STAGES_, int EPI_COLS_, int EPI_BUFS_, int PRODUCERS_>
+// buffers per epilogue warp (1 or 2)
+template <int BN_, int BK_, int STAGES_, int EPI_COLS_, int EPI_BUFS_>
 struct GemmConfig {
     static constexpr int BN = BN_;
     static constexpr int BK = BK_;
     static constexpr int kStages = STAGES_;
-    static constexpr int kProducers = PRODUCERS_;
-    static_assert(kProducers >= 1 && kProducers <= 4, "1 to 4 producer pairs");
-    // every ring slot must always be served by the same producer pair, so
-    // that a producer's last issue of a slot is that slot's last phase (the
-    // drain at the end waits on it)
-    static_assert(STAGES_ % PRODUCERS_ == 0, "stages must be a multiple of the producer pairs");
-    static constexpr int kPrefetchWarp = kFirstProducerWarp + 2 * kProducers;
+    static constexpr int kPrefetchWarp = kFirstLoaderWarp + kLoaderRoles;
     static constexpr int kThreads = 32 * (kPrefetchWarp + 1);
     static_assert(kThreads <= 1024, "too many warps");
     static constexpr int kEpiCols = EPI_COLS_;
@@ -124,8 +123,9 @@ struct GemmConfig {
     static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;  // 32 rows of one chunk
     static constexpr int kEpiOff = kStages * kStageBytes;
     static constexpr int kBarOff = kEpiOff + 4 * kEpiBufs * kEpiBufBytes;
-    // full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain, sf_drain
-    static constexpr int kNumBars = 3 * kStages + 6;
+    // full[S], empty[S], sf_ready[S], sf_full[S], acc_full[2], acc_empty[2],
+    // drain, sf_drain
+    static constexpr int kNumBars = 4 * kStages + 6;
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag, MMA progress
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
@@ -280,63 +280,63 @@ struct StageCursor {
     }
 };
 
-// One producer role: `IS_B` selects B (tile width BN, scales of BN/128 row
-// blocks) or A (128 rows, scales of one row block); the role serves the
-// stages q of this CTA's stage sequence with q % kProducers == cls.  The TMA
-// operations one thread issues complete about one after another, so the
-// stages are spread over several producer warps.  Arrives once per served
-// stage on full[slot] with the bytes it will deliver.
-template <class Cfg, bool IS_B>
-__device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base, uint32_t bar0,
-                                              const WaitCtx &wctx, int cls)
+// One loader role (one thread) of a CTA: ROLE 0 the A tile, 1 the B tile
+// (both complete on full[slot]), 2 the A scale atoms, 3 the B scale atoms
+// (both on sf_full[slot]).  One arrive.expect_tx and one TMA operation per
+// stage; boxes that reach past K or past the rows land as zeros and still
+// count their full size.
+template <class Cfg, int ROLE>
+__device__ __forceinline__ void loader_role(const KernelParams &kp, uint32_t base, uint32_t bar0,
+                                            const WaitCtx &wctx)
 {
+    const GemmParams &p = kp.g;
     constexpr int S = Cfg::kStages;
-    constexpr int ROWS = IS_B ? Cfg::BN : kBM;
-    constexpr int RB = ROWS / 128;                          // 128-row scale blocks per tile
-    constexpr uint32_t kTileOff = IS_B ? Cfg::kABytes : 0;
-    constexpr uint32_t kSfOff = Cfg::kABytes + Cfg::kBBytes + (IS_B ? Cfg::kSfaBytes : 0);
-    constexpr uint32_t kTileBytes = ROWS * Cfg::BK / 2;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    constexpr bool kSf = ROLE >= 2;
+    constexpr uint32_t kOff = ROLE == 0   ? 0u
+                              : ROLE == 1 ? (uint32_t)Cfg::kABytes
+                              : ROLE == 2 ? (uint32_t)(Cfg::kABytes + Cfg::kBBytes)
+                                          : (uint32_t)(Cfg::kABytes + Cfg::kBBytes + Cfg::kSfaBytes);
+    constexpr uint32_t kBytes = ROLE == 0   ? (uint32_t)Cfg::kABytes
+                                : ROLE == 1 ? (uint32_t)Cfg::kBBytes
+                                : ROLE == 2 ? (uint32_t)Cfg::kSfaBytes
+                                            : (uint32_t)Cfg::kSfbBytes;
+    // full[s] for the operand tiles, sf_full[s] for the scales
+    auto done_bar = [&](int s) { return bar0 + 8u * ((kSf ? 3 * S : 0) + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
 
-    const uint64_t pol = IS_B ? (p.b_policy == 1   ? ptx::policy_evict_first()
-                                 : p.b_policy == 2 ? ptx::policy_evict_last()
-                                                   : ptx::policy_evict_normal())
-                              : ptx::policy_evict_last();
+    const bool b_side = (ROLE == 1 || ROLE == 3);
+    const uint64_t pol = b_side ? (p.b_policy == 1   ? ptx::policy_evict_first()
+                                   : p.b_policy == 2 ? ptx::policy_evict_last()
+                                                     : ptx::policy_evict_normal())
+                                : ptx::policy_evict_last();
     uint32_t q = 0;   // position in this CTA's sequence of stages
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
     int g = 0;
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileCoord tc = tile_coord(p, t, g);
-        const int kchunks = p.kchunks[tc.g];
-        const int nst = stages_of<Cfg::BK>(kchunks);
-        const int kblk = kchunks * (kChunkK / kMmaK);      // scale atoms per row block
-        const int row0 = IS_B ? tc.bn * Cfg::BN : tc.bm * kBM;
-        const CUtensorMap *tm = IS_B ? &p.tmB[tc.g] : &p.tmA[tc.g];
-        const uint8_t *sf = (IS_B ? p.sfb[tc.g] : p.sfa[tc.g]) + (size_t)(row0 / 128) * kblk * 512;
+        const int nst = stages_of<Cfg::BK>(p.kchunks[tc.g]);
         for (int it = 0; it < nst; ++it, ++q) {
-            if ((int)(q % Cfg::kProducers) != cls)
-                continue;
             const int stage = (int)(q % S);
             const uint32_t phase = (q / S) & 1u;
             if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx, kRoleProducer)) {
                 ok = false;
                 break;
             }
-            const bool drop = IS_B && p.debug_drop_stage && blockIdx.x == 0 && q == 0;
+            const bool drop = ROLE == 1 && p.debug_drop_stage && blockIdx.x == 0 && q == 0;
             if (!drop) {
-                const int nk = kblocks_in_stage<Cfg::BK>(kchunks, it);
-                const uint32_t st = base + stage * Cfg::kStageBytes;
-                const uint32_t fb = full_bar(stage);
-                ptx::mbar_arrive_expect_tx(fb, kTileBytes + RB * nk * 512);
-                // the box always lands whole; chunks past K read as zeros
-                ptx::tma_load_3d(st + kTileOff, tm, 0, row0, it * Cfg::kChunks, fb, pol);
-#pragma unroll
-                for (int h = 0; h < RB; ++h)
-                    ptx::bulk_load(st + kSfOff + h * Cfg::kMmas * 512,
-                                   sf + ((size_t)h * kblk + (size_t)it * Cfg::kMmas) * 512,
-                                   nk * 512, fb, pol);
+                const uint32_t dst = base + stage * Cfg::kStageBytes + kOff;
+                const uint32_t bar = done_bar(stage);
+                ptx::mbar_arrive_expect_tx(bar, kBytes);
+                if (ROLE == 0)
+                    ptx::tma_load_3d(dst, &p.tmA[tc.g], 0, tc.bm * kBM, it * Cfg::kChunks, bar, pol);
+                else if (ROLE == 1)
+                    ptx::tma_load_3d(dst, &p.tmB[tc.g], 0, tc.bn * Cfg::BN, it * Cfg::kChunks, bar, pol);
+                else if (ROLE == 2)
+                    ptx::tma_load_3d(dst, &kp.tmSFA[tc.g], 0, it * Cfg::kMmas, tc.bm, bar, pol);
+                else
+                    ptx::tma_load_3d(dst, &kp.tmSFB[tc.g], 0, it * Cfg::kMmas, tc.bn * (Cfg::BN / 128),
+                                     bar, pol);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
@@ -345,11 +345,11 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
     // copies issued but never consumed (after an abort anywhere in the CTA)
     // still land in this CTA's shared memory: wait for the last issue of
     // every slot before the CTA can exit.  On the normal path these phases
-    // completed already (the MMA thread consumed them).
+    // completed already.
     (void)ok;
     for (int s = 0; s < S; ++s)
         if (issued & (1u << s))
-            wait_drain(full_bar(s), (issued_parity >> s) & 1u, wctx);
+            wait_drain(done_bar(s), (issued_parity >> s) & 1u, wctx);
 }
 
 // L2 prefetch role (one thread): walks this CTA's stage sequence and
@@ -359,9 +359,10 @@ __device__ __forceinline__ void producer_role(const GemmParams &p, uint32_t base
 // (without an error) when a wait for progress exceeds the wait timeout or
 // another role aborted.
 template <class Cfg>
-__device__ __forceinline__ void prefetch_role(const GemmParams &p, volatile uint32_t *progress,
+__device__ __forceinline__ void prefetch_role(const KernelParams &kp, volatile uint32_t *progress,
                                               const WaitCtx &wctx)
 {
+    const GemmParams &p = kp.g;
     const uint64_t pol = p.b_policy == 1   ? ptx::policy_evict_first()
                          : p.b_policy == 2 ? ptx::policy_evict_last()
                                            : ptx::policy_evict_normal();
@@ -377,14 +378,8 @@ __device__ __forceinline__ void prefetch_role(const GemmParams &p, volatile uint
                 __nanosleep(128);
             }
         }
-        const int kblk = p.kchunks[c.tc.g] * (kChunkK / kMmaK);
-        const int nk = kblocks_in_stage<Cfg::BK>(p.kchunks[c.tc.g], c.it);
         ptx::tma_prefetch_3d(&p.tmB[c.tc.g], 0, c.tc.bn * Cfg::BN, c.it * Cfg::kChunks, pol);
-#pragma unroll
-        for (int h = 0; h < Cfg::BN / 128; ++h)
-            ptx::bulk_prefetch(p.sfb[c.tc.g] + ((size_t)(c.tc.bn * (Cfg::BN / 128) + h) * kblk +
-                                                (size_t)c.it * Cfg::kMmas) * 512,
-                               nk * 512, pol);
+        ptx::tma_prefetch_3d(&kp.tmSFB[c.tc.g], 0, c.it * Cfg::kMmas, c.tc.bn * (Cfg::BN / 128), pol);
         c.advance(p);
         ++q;
     }
@@ -392,8 +387,9 @@ __device__ __forceinline__ void prefetch_role(const GemmParams &p, volatile uint
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
-    nvfp4_group_gemm_kernel(const __grid_constant__ GemmParams p)
+    nvfp4_group_gemm_kernel(const __grid_constant__ KernelParams kp)
 {
+    const GemmParams &p = kp.g;
     constexpr int BN = Cfg::BN;
     constexpr int S = Cfg::kStages;
     constexpr int EC = Cfg::kEpiCols;
@@ -407,10 +403,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * S + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
-    const uint32_t sf_drain_bar = bar0 + 8u * (3 * S + 5);
+    auto sffull_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (4 * S + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (4 * S + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (4 * S + 4);
+    const uint32_t sf_drain_bar = bar0 + 8u * (4 * S + 5);
     const uint32_t tmem_slot = base + Cfg::kSlotOff;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 4);
     volatile uint32_t *mma_progress = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 8);
@@ -420,9 +417,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(full_bar(s), 2);   // one A and one B producer per stage
+            ptx::mbar_init(full_bar(s), 2);     // the A and B loaders
             ptx::mbar_init(empty_bar(s), 1);
             ptx::mbar_init(sfr_bar(s), 1);
+            ptx::mbar_init(sffull_bar(s), 2);   // the A-scale and B-scale loaders
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
@@ -452,22 +450,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (warp == Cfg::kPrefetchWarp) {
         if (lane == 0 && p.pf_stages > 0)
-            prefetch_role<Cfg>(p, mma_progress, wctx);
-    } else if (warp >= kFirstProducerWarp) {
-        // producer warps: A, B, A, B, ... for stage classes 0, 0, 1, 1, ...
-        const int pw = warp - kFirstProducerWarp;
+            prefetch_role<Cfg>(kp, mma_progress, wctx);
+    } else if (warp >= kFirstLoaderWarp) {
         if (lane == 0) {
-            if (pw & 1)
-                producer_role<Cfg, true>(p, base, bar0, wctx, pw >> 1);
-            else
-                producer_role<Cfg, false>(p, base, bar0, wctx, pw >> 1);
+            switch (warp - kFirstLoaderWarp) {
+            case 0: loader_role<Cfg, 0>(kp, base, bar0, wctx); break;
+            case 1: loader_role<Cfg, 1>(kp, base, bar0, wctx); break;
+            case 2: loader_role<Cfg, 2>(kp, base, bar0, wctx); break;
+            default: loader_role<Cfg, 3>(kp, base, bar0, wctx); break;
+            }
         }
     } else if (warp == kSfWarp) {
         if (lane == 0) {
             // ------------------------------------------- scale copies
-            // once a stage's data has landed, copy its scale atoms into the
-            // slot's own tensor-memory columns and signal sf_ready[slot]; the
-            // MMA thread waits on that instead of full[slot]
+            // once a stage's scales have landed, copy the atoms into the
+            // slot's own tensor-memory columns and signal sf_ready[slot]
             uint32_t q = 0;
             bool ok = true, issued_any = false;
             int g = 0;
@@ -477,7 +474,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const int nst = stages_of<Cfg::BK>(kchunks);
                 for (int it = 0; it < nst; ++it, ++q) {
                     const int stage = (int)(q % S);
-                    if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
+                    if (!wait_bounded(sffull_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
                         ok = false;
                         break;
                     }
@@ -526,8 +523,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int it = 0; it < nst; ++it, ++q) {
                     const int stage = (int)(q % S);
-                    // sf_ready implies full: the scale thread waited for it
-                    if (!wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
+                    if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleMma) ||
+                        !wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
                         ok = false;
                         break;
                     }
@@ -682,13 +679,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 //   CfgWide512: BN = 256 with 512-K stages, 2 stages
 //   CfgCompute: BN = 128, 256-K stages, 4 stages, two 4 KiB staging buffers
 //               per warp (64-column stores)
-// The last parameter is the number of producer pairs.
 // ---------------------------------------------------------------------------
-using CfgStream = GemmConfig<128, 512, 3, 32, 1, 1>;
-using CfgWide = GemmConfig<256, 256, 4, 32, 1, 1>;
-using CfgWide512 = GemmConfig<256, 512, 2, 32, 1, 1>;
-using CfgCompute = GemmConfig<128, 256, 4, 64, 2, 1>;
-using CfgWideP2 = GemmConfig<256, 256, 4, 32, 1, 2>;
-using CfgWideP4 = GemmConfig<256, 256, 4, 32, 1, 4>;
+using CfgStream = GemmConfig<128, 512, 3, 32, 1>;
+using CfgWide = GemmConfig<256, 256, 4, 32, 1>;
+using CfgWide512 = GemmConfig<256, 512, 2, 32, 1>;
+using CfgCompute = GemmConfig<128, 256, 4, 64, 2>;
 
 }  // namespace nvfp4

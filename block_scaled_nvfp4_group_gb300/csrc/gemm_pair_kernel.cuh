@@ -16,15 +16,16 @@
 //        tensor memory in both CTAs;
 //   5    scale copier (even CTA, one thread): tcgen05.cp.cta_group::2 of the
 //        stage's scale atoms into both CTAs' tensor memory;
-//   6    A producer: this CTA's A tile [128 x 128 B] and its scale atoms;
-//   7    B producer: this CTA's half of the B tile [BN/2 x 128 B] and the
-//        scale atoms of the whole B tile (every CTA's tensor memory holds the
+//   6-9  loaders, one TMA thread and one operation per stage each: this CTA's
+//        A tile [128 x 128 B] and its half of the B tile [BN/2 x 128 B]
+//        (on full[slot]), this CTA's A scale atoms and the scale atoms of the
+//        whole B tile (on sf_full[slot]; every CTA's tensor memory holds the
 //        B scales of all BN columns);
-//   8    L2 prefetcher of this CTA's B half, paced by its B producer.
-// Loads of both CTAs complete on the even CTA's full[slot] barrier (TMA
-// .cta_group::2), whose two arrivals (the even CTA's producers) expect the
-// bytes of both CTAs; MMA completion is multicast to both CTAs' empty[slot]
-// and acc_full barriers.
+//   10   L2 prefetcher of this CTA's B half, paced by its B loader.
+// Loads of both CTAs complete on the even CTA's full / sf_full barriers (TMA
+// .cta_group::2), whose arrivals (the even CTA's loaders) expect the bytes of
+// both CTAs; MMA completion is multicast to both CTAs' empty[slot] and
+// acc_full barriers.
 //
 // The tile roles, descriptors and scale addressing follow kernelbot
 // nvfp4-group-gemm submission 474067 (group_gemm_persistent_kernel,
@@ -42,13 +43,9 @@
 
 namespace nvfp4 {
 
-struct PairParams {
-    // tmA: box {128, 128, 1} (this CTA's 128 rows); tmB: box {128, BN/2, 1};
-    // tmC as for one CTA; grid_m / tile_end count 256-row tiles
-    GemmParams g;
-    CUtensorMap tmSFA[kMaxGroups];  // uint32 {128, K/64, ceil(M/128)}, box {128, 4, 1}
-    CUtensorMap tmSFB[kMaxGroups];  // uint32 {128, K/64, ceil(N/128)}, box {128, 4, BN/128}
-};
+// Launches take KernelParams (gemm_kernel.cuh) with tmA: box {128, 128, 1}
+// (this CTA's 128 rows), tmB: box {128, BN/2, 1}, tmSFA box {128, 4, 1},
+// tmSFB box {128, 4, BN/128}; grid_m / tile_end count 256-row tiles.
 
 template <int BN_, int STAGES_, int EPI_COLS_>
 struct PairConfig {
@@ -68,21 +65,20 @@ struct PairConfig {
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KiB alignment");
     // bytes of one stage over both CTAs, as the even CTA's producers expect them
-    static constexpr uint32_t kTxA = 2u * (kABytes + kSfaBytes);
-    static constexpr uint32_t kTxB = 2u * (kBBytes + kSfbBytes);
+    static constexpr uint32_t kTx[4] = {2u * kABytes, 2u * kBBytes, 2u * kSfaBytes, 2u * kSfbBytes};
     static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
     static constexpr int kEpiOff = kStages * kStageBytes;
     static constexpr int kBarOff = kEpiOff + 4 * kEpiBufBytes;
-    // full[S], empty[S], sf_ready[S], acc_full, acc_empty, drain, sf_drain
-    static constexpr int kNumBars = 3 * kStages + 4;
+    // full[S], empty[S], sf_ready[S], sf_full[S], acc_full, acc_empty, drain,
+    // sf_drain
+    static constexpr int kNumBars = 4 * kStages + 4;
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag, B progress
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
     static constexpr int kMmaWarpP = 4;
     static constexpr int kSfWarpP = 5;
-    static constexpr int kAWarp = 6;
-    static constexpr int kBWarp = 7;
-    static constexpr int kPrefetchWarp = 8;
+    static constexpr int kFirstLoader = 6;   // A, B, A scales, B scales
+    static constexpr int kPrefetchWarp = 10;
     static constexpr int kThreads = 32 * (kPrefetchWarp + 1);
     static constexpr int kTmemCols = 512;
     static constexpr int kSfCol0 = BN;                     // one accumulator
@@ -112,26 +108,31 @@ __device__ __noinline__ bool wait_drain_ok(uint32_t bar, uint32_t parity, const 
     return true;
 }
 
-// One producer of one CTA of the pair: IS_B selects this CTA's half of the
-// B tile plus the scales of the whole B tile, else this CTA's A rows and
-// their scales.  Loads complete on the even CTA's full[slot]; only the even
-// CTA's producers arrive there (with the bytes of both CTAs).
-template <class Cfg, bool IS_B>
-__device__ __forceinline__ void pair_producer(const PairParams &pp, uint32_t base, uint32_t bar0,
-                                              uint32_t rank, volatile uint32_t *b_progress,
-                                              const WaitCtx &wctx)
+// One loader of one CTA of the pair: ROLE 0 this CTA's A rows, 1 this CTA's
+// half of the B tile (both on full[slot]), 2 this CTA's A scale atoms, 3 the
+// scale atoms of the whole B tile (both on sf_full[slot]).  Loads complete on
+// the even CTA's barrier; only the even CTA's loaders arrive there (with the
+// bytes of both CTAs).
+template <class Cfg, int ROLE>
+__device__ __forceinline__ void pair_loader(const KernelParams &kp, uint32_t base, uint32_t bar0,
+                                            uint32_t rank, volatile uint32_t *b_progress,
+                                            const WaitCtx &wctx)
 {
-    const GemmParams &p = pp.g;
+    const GemmParams &p = kp.g;
     constexpr int S = Cfg::kStages;
-    constexpr uint32_t kTileOff = IS_B ? Cfg::kABytes : 0;
-    constexpr uint32_t kSfOff = Cfg::kABytes + Cfg::kBBytes + (IS_B ? Cfg::kSfaBytes : 0);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    constexpr bool kSf = ROLE >= 2;
+    constexpr uint32_t kOff = ROLE == 0   ? 0u
+                              : ROLE == 1 ? (uint32_t)Cfg::kABytes
+                              : ROLE == 2 ? (uint32_t)(Cfg::kABytes + Cfg::kBBytes)
+                                          : (uint32_t)(Cfg::kABytes + Cfg::kBBytes + Cfg::kSfaBytes);
+    auto done_bar = [&](int s) { return bar0 + 8u * ((kSf ? 3 * S : 0) + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
 
-    const uint64_t pol = IS_B ? (p.b_policy == 1   ? ptx::policy_evict_first()
-                                 : p.b_policy == 2 ? ptx::policy_evict_last()
-                                                   : ptx::policy_evict_normal())
-                              : ptx::policy_evict_last();
+    const bool b_side = (ROLE == 1 || ROLE == 3);
+    const uint64_t pol = b_side ? (p.b_policy == 1   ? ptx::policy_evict_first()
+                                   : p.b_policy == 2 ? ptx::policy_evict_last()
+                                                     : ptx::policy_evict_normal())
+                                : ptx::policy_evict_last();
     const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
     uint32_t q = 0;
     uint32_t issued = 0, issued_parity = 0;
@@ -140,12 +141,6 @@ __device__ __forceinline__ void pair_producer(const PairParams &pp, uint32_t bas
     for (int t = pair; t < p.total_tiles && ok; t += npairs) {
         const TileCoord tc = tile_coord(p, t, g);
         const int nst = p.kchunks[tc.g];                    // one 256-K chunk per stage
-        const int row0 = IS_B ? tc.bn * Cfg::BN + (int)rank * (Cfg::BN / 2)
-                              : tc.bm * Cfg::kPairBM + (int)rank * kBM;
-        // 128-row scale block(s): this CTA's A block, or the B tile's first
-        const int rb0 = IS_B ? tc.bn * Cfg::kSfRb : tc.bm * 2 + (int)rank;
-        const CUtensorMap *tm = IS_B ? &p.tmB[tc.g] : &p.tmA[tc.g];
-        const CUtensorMap *tsf = IS_B ? &pp.tmSFB[tc.g] : &pp.tmSFA[tc.g];
         for (int it = 0; it < nst; ++it, ++q) {
             const int stage = (int)(q % S);
             const uint32_t phase = (q / S) & 1u;
@@ -153,32 +148,42 @@ __device__ __forceinline__ void pair_producer(const PairParams &pp, uint32_t bas
                 ok = false;
                 break;
             }
-            const bool drop = IS_B && p.debug_drop_stage && blockIdx.x == 0 && q == 0;
+            const bool drop = ROLE == 1 && p.debug_drop_stage && blockIdx.x == 0 && q == 0;
             if (!drop) {
-                const uint32_t st = base + stage * Cfg::kStageBytes;
-                const uint32_t fb_leader = ptx::mapa_shared(full_bar(stage), 0);
+                const uint32_t dst = base + stage * Cfg::kStageBytes + kOff;
+                const uint32_t bar_leader = ptx::mapa_shared(done_bar(stage), 0);
                 if (rank == 0)
-                    ptx::mbar_arrive_expect_tx(full_bar(stage), IS_B ? Cfg::kTxB : Cfg::kTxA);
-                ptx::tma_load_3d_pair(st + kTileOff, tm, 0, row0, it, fb_leader, pol);
-                ptx::tma_load_3d_pair(st + kSfOff, tsf, 0, it * Cfg::kMmas, rb0, fb_leader, pol);
+                    ptx::mbar_arrive_expect_tx(done_bar(stage), Cfg::kTx[ROLE]);
+                if (ROLE == 0)
+                    ptx::tma_load_3d_pair(dst, &p.tmA[tc.g], 0, tc.bm * Cfg::kPairBM + (int)rank * kBM, it,
+                                          bar_leader, pol);
+                else if (ROLE == 1)
+                    ptx::tma_load_3d_pair(dst, &p.tmB[tc.g], 0,
+                                          tc.bn * Cfg::BN + (int)rank * (Cfg::BN / 2), it, bar_leader, pol);
+                else if (ROLE == 2)
+                    ptx::tma_load_3d_pair(dst, &kp.tmSFA[tc.g], 0, it * Cfg::kMmas, tc.bm * 2 + (int)rank,
+                                          bar_leader, pol);
+                else
+                    ptx::tma_load_3d_pair(dst, &kp.tmSFB[tc.g], 0, it * Cfg::kMmas, tc.bn * Cfg::kSfRb,
+                                          bar_leader, pol);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
-            if (IS_B)
+            if (ROLE == 1)
                 *b_progress = q + 1;
         }
     }
     (void)ok;
     // Loads issued but not yet consumed still land in this CTA's shared
-    // memory.  The even CTA waits for its full[slot] phases (they count the
-    // bytes of both CTAs); the odd CTA cannot see those and waits instead for
-    // the MMAs to release its slots, giving up at the first expiry.
+    // memory.  The even CTA waits for its own barriers' phases (they count
+    // the bytes of both CTAs); the odd CTA cannot see those and waits instead
+    // for the MMAs to release its slots, giving up at the first expiry.
     bool alive = true;
     for (int s = 0; s < S && alive; ++s) {
         if (!(issued & (1u << s)))
             continue;
         const uint32_t par = (issued_parity >> s) & 1u;
-        alive = rank == 0 ? wait_drain_ok(full_bar(s), par, wctx)
+        alive = rank == 0 ? wait_drain_ok(done_bar(s), par, wctx)
                           : wait_drain_ok(empty_bar(s), par, wctx);
     }
 }
@@ -186,10 +191,10 @@ __device__ __forceinline__ void pair_producer(const PairParams &pp, uint32_t bas
 // L2 prefetch of this CTA's B half and its own B scale block, up to
 // `pf_stages` stages ahead of this CTA's B producer
 template <class Cfg>
-__device__ __forceinline__ void pair_prefetch(const PairParams &pp, uint32_t rank,
+__device__ __forceinline__ void pair_prefetch(const KernelParams &kp, uint32_t rank,
                                               volatile uint32_t *b_progress, const WaitCtx &wctx)
 {
-    const GemmParams &p = pp.g;
+    const GemmParams &p = kp.g;
     const uint64_t pol = p.b_policy == 1   ? ptx::policy_evict_first()
                          : p.b_policy == 2 ? ptx::policy_evict_last()
                                            : ptx::policy_evict_normal();
@@ -200,7 +205,7 @@ __device__ __forceinline__ void pair_prefetch(const PairParams &pp, uint32_t ran
         const TileCoord tc = tile_coord(p, t, g);
         const int nst = p.kchunks[tc.g];
         const int row0 = tc.bn * Cfg::BN + (int)rank * (Cfg::BN / 2);
-        const int rb = tc.bn * Cfg::kSfRb + (int)rank;
+        const int rb = tc.bn * Cfg::kSfRb;
         for (int it = 0; it < nst; ++it, ++q) {
             if (q >= *b_progress + (uint32_t)p.pf_stages) {
                 const uint64_t t0 = ptx::globaltimer_ns();
@@ -211,17 +216,17 @@ __device__ __forceinline__ void pair_prefetch(const PairParams &pp, uint32_t ran
                 }
             }
             ptx::tma_prefetch_3d(&p.tmB[tc.g], 0, row0, it, pol);
-            if (Cfg::kSfRb == 2)
-                ptx::tma_prefetch_3d(&pp.tmSFB[tc.g], 0, it * Cfg::kMmas, rb, pol);
+            if (rank == 0)
+                ptx::tma_prefetch_3d(&kp.tmSFB[tc.g], 0, it * Cfg::kMmas, rb, pol);
         }
     }
 }
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
-    nvfp4_group_gemm_pair_kernel(const __grid_constant__ PairParams pp)
+    nvfp4_group_gemm_pair_kernel(const __grid_constant__ KernelParams kp)
 {
-    const GemmParams &p = pp.g;
+    const GemmParams &p = kp.g;
     constexpr int BN = Cfg::BN;
     constexpr int S = Cfg::kStages;
     constexpr int EC = Cfg::kEpiCols;
@@ -235,10 +240,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    const uint32_t accf_bar = bar0 + 8u * (3 * S);
-    const uint32_t acce_bar = bar0 + 8u * (3 * S + 1);
-    const uint32_t drain_bar = bar0 + 8u * (3 * S + 2);
-    const uint32_t sf_drain_bar = bar0 + 8u * (3 * S + 3);
+    auto sffull_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+    const uint32_t accf_bar = bar0 + 8u * (4 * S);
+    const uint32_t acce_bar = bar0 + 8u * (4 * S + 1);
+    const uint32_t drain_bar = bar0 + 8u * (4 * S + 2);
+    const uint32_t sf_drain_bar = bar0 + 8u * (4 * S + 3);
     const uint32_t tmem_slot = base + Cfg::kSlotOff;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 4);
     volatile uint32_t *b_progress = reinterpret_cast<volatile uint32_t *>(gbase + Cfg::kSlotOff + 8);
@@ -249,9 +255,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(full_bar(s), 2);   // the even CTA's A and B producers
+            ptx::mbar_init(full_bar(s), 2);     // the even CTA's A and B loaders
             ptx::mbar_init(empty_bar(s), 1);
             ptx::mbar_init(sfr_bar(s), 1);
+            ptx::mbar_init(sffull_bar(s), 2);   // the even CTA's scale loaders
         }
         ptx::mbar_init(accf_bar, 1);
         ptx::mbar_init(acce_bar, 8);          // lane 0 of the 4 epilogue warps of both CTAs
@@ -280,13 +287,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
     if (warp == Cfg::kPrefetchWarp) {
         if (lane == 0 && p.pf_stages > 0)
-            pair_prefetch<Cfg>(pp, rank, b_progress, wctx);
-    } else if (warp == Cfg::kAWarp) {
-        if (lane == 0)
-            pair_producer<Cfg, false>(pp, base, bar0, rank, b_progress, wctx);
-    } else if (warp == Cfg::kBWarp) {
-        if (lane == 0)
-            pair_producer<Cfg, true>(pp, base, bar0, rank, b_progress, wctx);
+            pair_prefetch<Cfg>(kp, rank, b_progress, wctx);
+    } else if (warp >= Cfg::kFirstLoader) {
+        if (lane == 0) {
+            switch (warp - Cfg::kFirstLoader) {
+            case 0: pair_loader<Cfg, 0>(kp, base, bar0, rank, b_progress, wctx); break;
+            case 1: pair_loader<Cfg, 1>(kp, base, bar0, rank, b_progress, wctx); break;
+            case 2: pair_loader<Cfg, 2>(kp, base, bar0, rank, b_progress, wctx); break;
+            default: pair_loader<Cfg, 3>(kp, base, bar0, rank, b_progress, wctx); break;
+            }
+        }
     } else if (warp == Cfg::kSfWarpP) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------- scale copies
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const int nst = p.kchunks[tc.g];
                 for (int it = 0; it < nst; ++it, ++q) {
                     const int stage = (int)(q % S);
-                    if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
+                    if (!wait_bounded(sffull_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
                         ok = false;
                         break;
                     }
@@ -342,7 +352,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tc_fence_after();
                 for (int it = 0; it < nst; ++it, ++q) {
                     const int stage = (int)(q % S);
-                    if (!wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
+                    if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleMma) ||
+                        !wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
                         ok = false;
                         break;
                     }

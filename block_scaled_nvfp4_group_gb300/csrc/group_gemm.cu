@@ -37,6 +37,13 @@ bool needs_n256(int kind)
     return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4;
 }
 
+// the producer-pair variants are folded into WIDE: every stage's loads are
+// spread over four issuing warps in every configuration
+int canonical_kind(int kind)
+{
+    return (kind == kKindWideP2 || kind == kKindWideP4) ? kKindWide : kind;
+}
+
 // Launch configuration shared by every kind: programmatic stream
 // serialization (unless NVFP4_PDL=0), so the kernel may start while the
 // previous kernel in the stream finishes and waits for it
@@ -65,15 +72,15 @@ void make_launch_cfg(LaunchCfg &L, int grid, int threads, int smem, bool pair, c
 }
 
 template <class Cfg>
-cudaError_t launch_kind(const PairParams &P, int grid, cudaStream_t s)
+cudaError_t launch_kind(const KernelParams &P, int grid, cudaStream_t s)
 {
     LaunchCfg L;
     make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, false, s);
-    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg>, P.g);
+    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg>, P);
 }
 
 template <class Cfg>
-cudaError_t launch_pair_kind(const PairParams &P, int grid, cudaStream_t s)
+cudaError_t launch_pair_kind(const KernelParams &P, int grid, cudaStream_t s)
 {
     LaunchCfg L;
     make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, true, s);
@@ -85,27 +92,29 @@ struct KindInfo {
     int bn;
     int box_b;      // rows of B one CTA loads per stage
     int chunks;     // 128-byte K chunks per row per stage
+    int sf_atoms;   // scale atoms per row block per stage (stage K / 64)
+    int sfb_blocks; // 128-row scale blocks of B per stage
     int epi_cols;
     int threads;
     int smem;
     bool pair;
     const void *fn;
-    cudaError_t (*launch)(const PairParams &, int, cudaStream_t);
+    cudaError_t (*launch)(const KernelParams &, int, cudaStream_t);
 };
 
 template <class Cfg>
 KindInfo make_kind()
 {
-    return KindInfo{kBM, Cfg::BN, Cfg::BN, Cfg::kChunks, Cfg::kEpiCols, Cfg::kThreads,
-                    Cfg::kSmemBytes, false,
+    return KindInfo{kBM, Cfg::BN, Cfg::BN, Cfg::kChunks, Cfg::kMmas, Cfg::BN / 128, Cfg::kEpiCols,
+                    Cfg::kThreads, Cfg::kSmemBytes, false,
                     reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg>), &launch_kind<Cfg>};
 }
 
 template <class Cfg>
 KindInfo make_pair_kind()
 {
-    return KindInfo{Cfg::kPairBM, Cfg::BN, Cfg::BN / 2, 1, Cfg::kEpiCols, Cfg::kThreads,
-                    Cfg::kSmemBytes, true,
+    return KindInfo{Cfg::kPairBM, Cfg::BN, Cfg::BN / 2, 1, Cfg::kMmas, Cfg::kSfRb, Cfg::kEpiCols,
+                    Cfg::kThreads, Cfg::kSmemBytes, true,
                     reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg>),
                     &launch_pair_kind<Cfg>};
 }
@@ -113,10 +122,10 @@ KindInfo make_pair_kind()
 const KindInfo &kind_info(int k)
 {
     static const KindInfo table[kNumKinds] = {
-        make_kind<CfgStream>(),  make_kind<CfgWide>(),  make_kind<CfgCompute>(),
-        make_kind<CfgWide512>(), make_kind<CfgWideP2>(), make_kind<CfgWideP4>(),
+        make_kind<CfgStream>(),  make_kind<CfgWide>(), make_kind<CfgCompute>(),
+        make_kind<CfgWide512>(), make_kind<CfgWide>(), make_kind<CfgWide>(),
         make_pair_kind<CfgPair>()};
-    return table[k];
+    return table[canonical_kind(k)];
 }
 
 std::mutex g_attr_mu;
@@ -276,7 +285,7 @@ template <class ErrFn>
 int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
                     int sm_count, int kind, ErrFn err_for_launch)
 {
-    static thread_local std::vector<PairParams> plist;
+    static thread_local std::vector<KernelParams> plist;
     const KindInfo &ki = kind_info(kind);
     const int b_policy = choose_b_policy();
     const int pf = choose_prefetch();
@@ -296,7 +305,7 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         if (plist.empty() || plist.back().g.num_groups == kMaxGroups ||
             plist.back().g.total_tiles + tiles > kMaxTilesPerLaunch) {
             plist.emplace_back();
-            std::memset(&plist.back(), 0, sizeof(PairParams));
+            std::memset(&plist.back(), 0, sizeof(KernelParams));
             GemmParams &P = plist.back().g;
             P.err = err_for_launch((int)plist.size() - 1);
             P.timeout_ns = timeout;
@@ -304,22 +313,21 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
             P.pf_stages = pf;
             P.debug_drop_stage = drop;
         }
-        PairParams &PP = plist.back();
+        KernelParams &PP = plist.back();
         GemmParams &P = PP.g;
         const int j = P.num_groups;
         rc = encode_map_operand(&P.tmA[j], g.A, (uint64_t)g.M, (uint64_t)g.K, kBM, ki.chunks);
         if (rc == NVFP4_OK)
             rc = encode_map_operand(&P.tmB[j], g.B, (uint64_t)g.N, (uint64_t)g.K, ki.box_b,
                                     ki.chunks);
-        if (rc == NVFP4_OK && ki.pair)
-            rc = encode_map_sf(&PP.tmSFA[j], g.SFA, (uint64_t)g.M, (uint64_t)g.K, 1);
-        if (rc == NVFP4_OK && ki.pair)
-            rc = encode_map_sf(&PP.tmSFB[j], g.SFB, (uint64_t)g.N, (uint64_t)g.K, ki.bn / 128);
+        if (rc == NVFP4_OK)
+            rc = encode_map_sf(&PP.tmSFA[j], g.SFA, (uint64_t)g.M, (uint64_t)g.K, ki.sf_atoms, 1);
+        if (rc == NVFP4_OK)
+            rc = encode_map_sf(&PP.tmSFB[j], g.SFB, (uint64_t)g.N, (uint64_t)g.K, ki.sf_atoms,
+                               ki.sfb_blocks);
         if (rc == NVFP4_OK)
             rc = encode_map_2d(&P.tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
                                (uint64_t)g.M, (uint64_t)g.N * 2, ki.epi_cols, 32, c_swizzle);
-        P.sfa[j] = static_cast<const uint8_t *>(g.SFA);
-        P.sfb[j] = static_cast<const uint8_t *>(g.SFB);
         P.M[j] = g.M;
         P.N[j] = g.N;
         P.kchunks[j] = g.K / kChunkK;
@@ -329,7 +337,7 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         P.num_groups = j + 1;
     }
     for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
-        const PairParams &P = plist[l];
+        const KernelParams &P = plist[l];
         const int grid = grid_size(dev, kind, P.g.total_tiles, sm_count);
         if (ki.launch(P, grid, stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
             rc = NVFP4_ERR_CUDA;

@@ -162,10 +162,11 @@ int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_
     return encode_map(out, key);
 }
 
-int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_blocks)
+int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_atoms,
+                  uint32_t box_blocks)
 {
     const uint64_t atoms = K / 64;
-    const MapKey key{ptr, 128, atoms, (rows + 127) / 128, 512, atoms * 512, 128, 4, box_blocks, 3,
+    const MapKey key{ptr, 128, atoms, (rows + 127) / 128, 512, atoms * 512, 128, box_atoms, box_blocks, 3,
                      (int)CU_TENSOR_MAP_DATA_TYPE_UINT32, (int)CU_TENSOR_MAP_SWIZZLE_NONE};
     return encode_map(out, key);
 }

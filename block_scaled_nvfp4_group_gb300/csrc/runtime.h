@@ -36,9 +36,11 @@ int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_
 
 // Tiled scale factors of a [rows][K] operand (ceil(rows/128) row blocks of
 // K/64 atoms of 512 bytes) as a 3-D uint32 tensor {128, K/64, row blocks},
-// box {128, 4, box_blocks}, no swizzle: one load brings the 4 atoms of one
-// 256-K stage for box_blocks consecutive row blocks (zeros past the last).
-int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_blocks);
+// box {128, box_atoms, box_blocks}, no swizzle: one load brings the atoms of
+// one stage (box_atoms = stage K / 64) for box_blocks consecutive row blocks
+// (zeros past the last atom or row block).
+int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_atoms,
+                  uint32_t box_blocks);
 
 unsigned long long wait_timeout_ns();
 int debug_drop_stage();

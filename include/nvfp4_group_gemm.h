@@ -83,7 +83,8 @@ int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t strea
  *  WIDE    128 x 256 tiles, 256-K stages (every N a multiple of 256)
  *  COMPUTE 128 x 128 tiles, 256-K stages, 64-column stores
  *  WIDE512 128 x 256 tiles, 512-K stages
- *  WIDE_P2 / WIDE_P4  WIDE with two / four producer pairs
+ *  WIDE_P2 / WIDE_P4  accepted for compatibility; the same as WIDE (every
+ *          configuration spreads a stage's loads over four issuing warps)
  *  PAIR    256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; N >= 256):
  *          chosen for large M, when pairing fills at least four rounds of
  *          the grid without adding one */
