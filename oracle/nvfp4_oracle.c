@@ -449,3 +449,108 @@ int nvfp4_oracle_sf_unrelayout(const uint8_t *tiled, uint8_t *dst, int rows, int
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 quantisation, the step that produces the GEMM's operands: every    */
+/* 16-element block of a row gets the scale E4M3FN(absmax / 6) and every    */
+/* element the E2M1 code of x / scale (the generator of the "quantized"     */
+/* configuration of the grouped GEMM: values quantised per 16-block to E2M1 */
+/* with an absmax/6 scale rounded to E4M3FN).  Both rounding decisions are  */
+/* taken on IEEE single-precision values (absmax / 6 and x / scale rounded  */
+/* to nearest), the precision the GPU kernel computes in.                   */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary16 bits -> float (exact: every half is a float) */
+static float half_bits_to_float(uint16_t h)
+{
+    const unsigned s = (h >> 15) & 1u, e = (h >> 10) & 31u, m = h & 1023u;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                       /* subnormal */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1.0 + (double)m / 1024.0, (int)e - 15);
+    return (float)(s ? -v : v);
+}
+
+/* bfloat16 bits -> float (exact: the upper half of a float's bits) */
+static float bf16_bits_to_float(uint16_t h)
+{
+    const uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof(f));
+    return f;
+}
+
+/* E4M3FN code of a finite float >= 0: the nearest finite E4M3FN value, ties
+ * to the even code (mantissa bit 0 clear); everything above 448 becomes 448
+ * (0x7E), the largest finite value; 0 and negative inputs give 0. */
+unsigned nvfp4_oracle_e4m3_rne(float v)
+{
+    if (!(v > 0.0f))
+        return 0;
+    const double x = (double)v;
+    unsigned best = 0;
+    double best_d = x;                                    /* distance to 0 */
+    for (unsigned c = 1; c < 0x7F; ++c) {                 /* 0x7F is NaN */
+        const double d = fabs(x - nvfp4_oracle_e4m3fn(c));
+        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* E2M1 code of a finite float: the magnitude is the nearest of
+ * {0, .5, 1, 1.5, 2, 3, 4, 6} (ties to the even code, 6 for anything larger),
+ * the sign goes to bit 3 unless the magnitude is 0 (zero is always 0x0). */
+unsigned nvfp4_oracle_e2m1_rne(float q)
+{
+    const double a = fabs((double)q);
+    unsigned best = 0;
+    double best_d = a;
+    for (unsigned c = 1; c < 8; ++c) {
+        const double d = fabs(a - nvfp4_oracle_e2m1(c));
+        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (best != 0 && q < 0.0f) ? (best | 8u) : best;
+}
+
+/* x: [rows][K] FP16 (is_bf16 = 0) or BF16 (is_bf16 = 1) bits, finite;
+ * codes: [rows][K/2] bytes, element 2i in the low nibble; sf: [rows][K/16]
+ * E4M3FN bytes (row-major).  A block whose scale rounds to 0 (absmax < 6 *
+ * 2^-10, all zeros included) gets scale 0 and codes 0.  K % 16 == 0. */
+int nvfp4_oracle_quantize(const uint16_t *x, int is_bf16, int rows, int K, uint8_t *codes,
+                          uint8_t *sf)
+{
+    if (rows < 0 || K <= 0 || K % 16 != 0 || !x || !codes || !sf)
+        return -1;
+    for (int r = 0; r < rows; ++r) {
+        for (int b = 0; b < K / 16; ++b) {
+            float v[16];
+            float amax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                const uint16_t h = x[(size_t)r * K + (size_t)b * 16 + i];
+                v[i] = is_bf16 ? bf16_bits_to_float(h) : half_bits_to_float(h);
+                const float a = fabsf(v[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            const float s32 = amax / 6.0f;
+            const unsigned sc = nvfp4_oracle_e4m3_rne(s32);
+            const float sdec = (float)nvfp4_oracle_e4m3fn(sc);
+            sf[(size_t)r * (K / 16) + b] = (uint8_t)sc;
+            for (int i = 0; i < 16; i += 2) {
+                const unsigned lo = sdec > 0.0f ? nvfp4_oracle_e2m1_rne(v[i] / sdec) : 0u;
+                const unsigned hi = sdec > 0.0f ? nvfp4_oracle_e2m1_rne(v[i + 1] / sdec) : 0u;
+                codes[(size_t)r * (K / 2) + (size_t)b * 8 + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return 0;
+}

@@ -9,8 +9,10 @@ The oracle computes, for one group,
 e2m1(B[n][k]) * e4m3fn(SFB[n][k//16]))`` in float64 (kernelbot
 nvfp4-group-gemm submission 474067: header comment of the CUDA source and
 ``tcgen05_mma_nvfp4``, ``kind::mxf4nvf4.block_scale.block16``), with plain
-row-major scale factors, and defines the tiled scale-factor layout the GPU
-kernel reads.
+row-major scale factors, defines the tiled scale-factor layout the GPU
+kernel reads, and the NVFP4 quantisation that produces the operands
+(per 16-block scale E4M3FN(absmax/6), codes E2M1(x/scale), decisions taken on
+IEEE single-precision values).
 """
 from __future__ import annotations
 
@@ -94,6 +96,12 @@ class Oracle:
         L.nvfp4_oracle_sf_relayout.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int]
         L.nvfp4_oracle_sf_unrelayout.restype = ctypes.c_int
         L.nvfp4_oracle_sf_unrelayout.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int]
+        L.nvfp4_oracle_e4m3_rne.restype = ctypes.c_uint
+        L.nvfp4_oracle_e4m3_rne.argtypes = [ctypes.c_float]
+        L.nvfp4_oracle_e2m1_rne.restype = ctypes.c_uint
+        L.nvfp4_oracle_e2m1_rne.argtypes = [ctypes.c_float]
+        L.nvfp4_oracle_quantize.restype = ctypes.c_int
+        L.nvfp4_oracle_quantize.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u8p, _u8p]
         self.L = L
         self.path = path
 
@@ -168,6 +176,25 @@ class Oracle:
         Returns a list of uint16 [M, N] arrays of FP16 bits."""
         return [self.gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, threads=threads)
                 for g in groups]
+
+    # quantisation ---------------------------------------------------------------
+    def e4m3_rne(self, v: float) -> int:
+        return int(self.L.nvfp4_oracle_e4m3_rne(float(v)))
+
+    def e2m1_rne(self, q: float) -> int:
+        return int(self.L.nvfp4_oracle_e2m1_rne(float(q)))
+
+    def quantize(self, x_bits, rows: int, K: int, bf16: bool = False):
+        """x_bits: uint16 [rows, K] FP16 (or BF16) bits.  Returns (codes
+        uint8 [rows, K/2], row-major E4M3FN scales uint8 [rows, K/16])."""
+        x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
+        assert x.size == rows * K
+        codes = np.zeros((rows, K // 2), dtype=np.uint8)
+        sf = np.zeros((rows, K // 16), dtype=np.uint8)
+        if rows and self.L.nvfp4_oracle_quantize(_p(x, _u16p), 1 if bf16 else 0, rows, K,
+                                                 _p(codes, _u8p), _p(sf, _u8p)) != 0:
+            raise ValueError("oracle quantize failed")
+        return codes, sf
 
     # scale-factor layout ------------------------------------------------------
     def sf_tiled_bytes(self, rows: int, K: int) -> int:

@@ -334,9 +334,118 @@ def check_relayout(o, seed=19):
         assert nz.tolist() == [off], (rows, K, r, j, nz[:4], off)
 
 
+# --- NVFP4 quantisation --------------------------------------------------
+
+def _f32(v):
+    return float(np.float32(v))
+
+
+def check_quant_e4m3_vs_torch(o, seed=21):
+    """The scale rounding against PyTorch's float8_e4m3fn conversion (round
+    to nearest even) on random in-range values and on every exact midpoint
+    between neighbouring E4M3FN values; above 448 the oracle saturates."""
+    rng = np.random.default_rng(seed)
+    vals = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(440.0), size=2000)).astype(np.float32)
+    pts = sorted(golden_e4m3_points().items())
+    pos = sorted(v for _, v in pts if 0 < v < float("inf") and v == v)
+    grid = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    vals = np.concatenate([vals, mids, np.array(pos, dtype=np.float32)])
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([o.e4m3_rne(float(v)) for v in vals], dtype=np.uint8)
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:5]]
+    for v in (448.0, 449.0, 464.0, 1e6):
+        assert o.e4m3_rne(v) == 0x7E, v
+    assert o.e4m3_rne(0.0) == 0 and o.e4m3_rne(-3.0) == 0
+
+
+# q -> E2M1 code, from the grid {0, .5, 1, 1.5, 2, 3, 4, 6} written out by
+# hand: nearest value, ties to the even code, 6 above, zero without sign
+_E2M1_CASES = [
+    (0.0, 0x0), (0.24, 0x0), (0.25, 0x0), (0.26, 0x1), (0.5, 0x1), (0.74, 0x1), (0.75, 0x2),
+    (1.25, 0x2), (1.26, 0x3), (1.75, 0x4), (2.49, 0x4), (2.5, 0x4), (2.51, 0x5), (3.49, 0x5),
+    (3.5, 0x6), (4.99, 0x6), (5.0, 0x6), (5.01, 0x7), (6.0, 0x7), (100.0, 0x7),
+    (-0.1, 0x0), (-0.25, 0x0), (-0.3, 0x9), (-1.75, 0xC), (-6.5, 0xF), (-3.0, 0xD),
+]
+
+
+def check_quant_e2m1_rounding(o):
+    for q, code in _E2M1_CASES:
+        got = o.e2m1_rne(q)
+        assert got == code, (q, got, code)
+
+
+def _half_bits(vals):
+    return np.asarray(vals, dtype=np.float16).view(np.uint16)
+
+
+def check_quant_blocks(o):
+    """Hand-made blocks: exact scale 1 (absmax 6), an all-zero block, a block
+    whose scale rounds to zero, a saturating block, a negative absmax, and the
+    nibble order; FP16 and BF16 inputs of the same values agree."""
+    K = 64
+    x = np.zeros((2, K), dtype=np.float32)
+    x[0, 0:16] = [6, -6, 3, 1.5, 0.5, -0.25, 0.75, 2, 0, 1, -1, 4, 5, 2.5, -3.5, 0.1]
+    # block 1 of row 0 stays zero
+    x[0, 32:48] = 0.005                     # absmax / 6 < 2^-10: scale 0
+    x[0, 48:64] = [60000] + [1000] * 15     # scale saturates at 448
+    x[1, 0:16] = [-12] + [1] * 15           # negative absmax: scale 2
+    x[1, 16:32] = np.arange(16)            # scale 15/6 = 2.5
+    for bf16 in (False, True):
+        if bf16:
+            bits = (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        else:
+            bits = _half_bits(x)
+        codes, sf = o.quantize(bits, 2, K, bf16=bf16)
+        assert sf[0].tolist() == [0x38, 0x00, 0x00, 0x7E], sf[0]
+        assert sf[1, 0] == 0x40 and sf[1, 1] == 0x42, sf[1]     # 2.0, 2.5
+        lo = codes[0, :8] & 0xF
+        hi = codes[0, :8] >> 4
+        first = np.empty(16, dtype=np.uint8)
+        first[0::2], first[1::2] = lo, hi
+        # 6,-6,3,1.5,.5,-.25,.75,2,0,1,-1,4,5,2.5,-3.5,.1 -> codes
+        assert first.tolist() == [0x7, 0xF, 0x5, 0x3, 0x1, 0x0, 0x2, 0x4,
+                                  0x0, 0x2, 0xA, 0x6, 0x6, 0x4, 0xE, 0x0], first
+        assert not codes[0, 8:24].any()                 # zero block and scale-0 block
+        assert (codes[0, 24] & 0xF) == 0x7 and (codes[0, 24] >> 4) == 0x4   # 60000/448 -> 6, 1000/448 = 2.23 -> 2
+        # row 1 block 0: -12/2 = -6 -> 0xF, 1/2 = .5 -> 0x1
+        assert codes[1, 0] == (0xF | (0x1 << 4))
+        # row 1 block 1: i / 2.5 for i = 0..15
+        exp = [o.e2m1_rne(np.float32(i) / np.float32(2.5)) for i in range(16)]
+        got = [(codes[1, 8 + i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+        assert got == exp, (got, exp)
+
+
+def check_quant_vs_float64_generator(o, seed=23):
+    """Against the workloads' own per-block quantiser (float64 decisions,
+    written independently): on Gaussian FP16 inputs every scale and all but
+    rare rounding-boundary codes agree, and no code is off by more than one
+    grid step."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from block_scaled_nvfp4_group_gb300 import workloads
+    rng = np.random.default_rng(seed)
+    rows, K = 64, 1024
+    x16 = rng.standard_normal((rows, K)).astype(np.float16)
+    codes, sf = o.quantize(x16.view(np.uint16), rows, K)
+    c64, s64 = workloads.quantize_nvfp4(x16.astype(np.float64))
+    assert (sf == s64).mean() > 0.999, (sf != s64).sum()
+    same = sf == s64
+    a = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(rows, K)
+    b = np.stack([c64 & 0xF, c64 >> 4], axis=-1).reshape(rows, K)
+    blockok = np.repeat(same, 16, axis=1)
+    diff = (a != b) & blockok
+    assert diff.mean() < 1e-3, diff.sum()
+    mag = lambda c: c & 7
+    assert (np.abs(mag(a[diff]).astype(int) - mag(b[diff]).astype(int)) <= 1).all()
+
+
 ALL_CHECKS = [
     check_e2m1_table, check_e4m3_all_codes, check_fp16_rounding, check_brute_force_tiny,
     check_brute_force_grouped, check_fixed_point, check_single_nonzero,
     check_all_ones_power_of_two, check_zero_scales, check_nibble_order, check_scale_blocks,
     check_signs, check_row_and_column_split, check_transpose_symmetry, check_relayout,
+    check_quant_e4m3_vs_torch, check_quant_e2m1_rounding, check_quant_blocks,
+    check_quant_vs_float64_generator,
 ]

@@ -61,6 +61,28 @@ MUTANTS = {
     "atom_order_k_major": (
         "((size_t)rb * kblocks + kb) * 512",
         "((size_t)kb * ((rows + 127) / 128) + rb) * 512"),
+    "quant_scale_over_4": (
+        "const float s32 = amax / 6.0f;",
+        "const float s32 = amax / 4.0f;"),
+    "quant_absmax_signed": (
+        "const float a = fabsf(v[i]);",
+        "const float a = v[i];"),
+    "quant_nibbles_swapped": (
+        "(uint8_t)(lo | (hi << 4));",
+        "(uint8_t)(hi | (lo << 4));"),
+    "quant_negative_zero": (
+        "return (best != 0 && q < 0.0f) ? (best | 8u) : best;",
+        "return (q < 0.0f) ? (best | 8u) : best;"),
+    "quant_e2m1_ties_up": (
+        "    for (unsigned c = 1; c < 8; ++c) {\n        const double d = fabs(a - nvfp4_oracle_e2m1(c));\n"
+        "        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {",
+        "    for (unsigned c = 1; c < 8; ++c) {\n        const double d = fabs(a - nvfp4_oracle_e2m1(c));\n"
+        "        if (d <= best_d) {"),
+    "quant_e4m3_truncates": (
+        "        const double d = fabs(x - nvfp4_oracle_e4m3fn(c));\n"
+        "        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {",
+        "        const double d = fabs(x - nvfp4_oracle_e4m3fn(c));\n"
+        "        if (nvfp4_oracle_e4m3fn(c) <= x) {"),
     "fixed_point_shift": (
         "int shift = ea + eb - 2 + 20;",
         "int shift = ea + eb - 1 + 20;"),
