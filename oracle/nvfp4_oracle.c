@@ -490,6 +490,8 @@ unsigned nvfp4_oracle_e4m3_rne(float v)
 {
     if (!(v > 0.0f))
         return 0;
+    if (v >= 448.0f)          /* saturation (also keeps the distances below exact) */
+        return 0x7E;
     const double x = (double)v;
     unsigned best = 0;
     double best_d = x;                                    /* distance to 0 */
@@ -509,6 +511,8 @@ unsigned nvfp4_oracle_e4m3_rne(float v)
 unsigned nvfp4_oracle_e2m1_rne(float q)
 {
     const double a = fabs((double)q);
+    if (a >= 6.0)             /* saturation (also keeps the distances below exact) */
+        return q < 0.0f ? 0xFu : 0x7u;
     unsigned best = 0;
     double best_d = a;
     for (unsigned c = 1; c < 8; ++c) {

@@ -355,7 +355,7 @@ def check_quant_e4m3_vs_torch(o, seed=21):
     got = np.array([o.e4m3_rne(float(v)) for v in vals], dtype=np.uint8)
     bad = np.flatnonzero(got != ref)
     assert bad.size == 0, [(float(vals[i]), int(got[i]), int(ref[i])) for i in bad[:5]]
-    for v in (448.0, 449.0, 464.0, 1e6):
+    for v in (448.0, 449.0, 464.0, 1e6, 5e37, 3.4e38):
         assert o.e4m3_rne(v) == 0x7E, v
     assert o.e4m3_rne(0.0) == 0 and o.e4m3_rne(-3.0) == 0
 
@@ -367,6 +367,7 @@ _E2M1_CASES = [
     (1.25, 0x2), (1.26, 0x3), (1.75, 0x4), (2.49, 0x4), (2.5, 0x4), (2.51, 0x5), (3.49, 0x5),
     (3.5, 0x6), (4.99, 0x6), (5.0, 0x6), (5.01, 0x7), (6.0, 0x7), (100.0, 0x7),
     (-0.1, 0x0), (-0.25, 0x0), (-0.3, 0x9), (-1.75, 0xC), (-6.5, 0xF), (-3.0, 0xD),
+    (1e30, 0x7), (-1e30, 0xF), (6.7e35, 0x7),
 ]
 
 
