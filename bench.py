@@ -445,6 +445,117 @@ def run_profile(args):
         sys.exit(1)
 
 
+def quantize_input(wl, seed: int) -> np.ndarray:
+    """The rows the quantisation kernel is timed on: one FP16 matrix holding
+    the A operands (activations) of every group of the workload, Gaussian
+    values, [sum(M_g), K]."""
+    rows = sum(g.M for g in wl.groups)
+    K = wl.groups[0].K
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((rows, K)).astype(np.float16)
+
+
+def run_quantize(args):
+    """NVFP4 quantisation of the workload's activations: one launch per step
+    (FP16 [sum M_g, K] -> codes + tiled scales), inputs resident, CUDA graph
+    replay with the L2 flushed before every step; HBM roofline."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from block_scaled_nvfp4_group_gb300 import ops, workloads
+    wl = workloads.make_workload(args.workload)
+    x16 = quantize_input(wl, wl.seed + 104729)
+    rows, K = x16.shape
+    x = torch.from_numpy(x16).to(dev)
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=dev)
+    tiled = torch.empty(ops.sf_tiled_bytes(rows, K), dtype=torch.uint8, device=dev)
+    nbytes = rows * K * 2 + rows * K // 2 + ops.sf_tiled_bytes(rows, K)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ops.quantize(x, codes=codes, sf_tiled=tiled)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if args.profile:
+        print(json.dumps({"profile": "quantize_" + args.workload, "device_error": ops.last_device_error()}))
+        return
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.15)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    w0 = time.time()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    ms_mean = sum(ms) / len(ms)
+    ms_med = statistics.median(ms)
+    # end to end through the public API: pinned H2D of x, the launch, D2H of
+    # codes and tiled scales
+    xh = torch.from_numpy(x16).pin_memory()
+    ch = torch.empty(codes.shape, dtype=torch.uint8).pin_memory()
+    th = torch.empty(tiled.shape, dtype=torch.uint8).pin_memory()
+    n_e2e = min(args.steps, 100)
+    e2e = []
+    for _ in range(n_e2e):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(xh, non_blocking=True)
+        step()
+        ch.copy_(codes, non_blocking=True)
+        th.copy_(tiled, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e.append(a.elapsed_time(b))
+    e2e_ms = statistics.median(e2e)
+    peaks = load_peaks()
+    gbs = nbytes / (ms_mean * 1e-3) / 1e9
+    line = {
+        "metric": "NVFP4 quantisation GB/s (FP16 in, codes + tiled scales out)", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_mean, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"quantize_{args.workload}_activations", "rows": rows, "K": K,
+                   "l2": "flushed by a 512 MiB device write before every timed step"},
+        "us_per_call": {"mean": ms_mean * 1e3, "median": ms_med * 1e3},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms_med * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": nbytes / (ms_med * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "kernel": "quantize_kernel",
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "peak_source": peaks["source"] + " (hbm_gbs)"},
+        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": rows * K * 2,
+                "d2h_bytes_per_step": codes.numel() + tiled.numel(), "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        from oracle import oracle
+        o = oracle.get()
+        sample = min(rows, 256)
+        t0 = time.time()
+        o.quantize(x16[:sample].view(np.uint16), sample, K)
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": sample * K * (2 + 0.5 + 1 / 16) / dt / 1e9, "unit": "GB/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": f"{sample} of {rows} rows, {dt:.2f} s"}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,10 +568,19 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
     ap.add_argument("--profile", action="store_true",
                     help="few launches for ncu: W warm-up steps, then one step")
+    ap.add_argument("--op", default="gemm", choices=["gemm", "quantize"],
+                    help="gemm: the relayout + grouped GEMM step (default); quantize: the "
+                         "NVFP4 quantisation of the workload's activations")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.op == "quantize":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "quantize",
+                              "unavailable": "the reference arm times the GEMM oracle"}))
+            return
+        run_quantize(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.profile:
         run_profile(args)

@@ -51,6 +51,9 @@ SIGNATURES = {
     "nvfp4_sf_relayout_group": (ctypes.c_int, [ctypes.POINTER(SfRelayoutDesc), ctypes.c_int,
                                                ctypes.c_void_p]),
     "nvfp4_sf_tiled_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int]),
+    "nvfp4_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p]),
     "nvfp4_last_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "nvfp4_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "nvfp4_debug_drop_first_stage": (None, [ctypes.c_int]),

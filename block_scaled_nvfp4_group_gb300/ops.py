@@ -109,6 +109,28 @@ def group_gemm_plan(groups=None, descs=None):
     return _abi.KIND_NAMES[kind.value], launches.value
 
 
+def quantize(x: torch.Tensor, codes: torch.Tensor | None = None, sf_tiled: torch.Tensor | None = None,
+             sf_rowmajor: torch.Tensor | None = None, want_rowmajor: bool = False, stream=None):
+    """NVFP4 quantisation of a [rows, K] float16 / bfloat16 CUDA tensor (see
+    nvfp4_quantize): returns (codes uint8 [rows, K/2], tiled scales uint8,
+    row-major scales uint8 [rows, K/16] or None)."""
+    if x.dtype not in (torch.float16, torch.bfloat16) or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D float16 or bfloat16 tensor")
+    rows, K = x.shape
+    if codes is None:
+        codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    if sf_tiled is None:
+        sf_tiled = torch.empty(max(sf_tiled_bytes(rows, K), 16), dtype=torch.uint8, device=x.device)
+    if sf_rowmajor is None and want_rowmajor:
+        sf_rowmajor = torch.empty((rows, K // 16), dtype=torch.uint8, device=x.device)
+    lib = _abi.load()
+    _abi.check(lib.nvfp4_quantize(x.data_ptr(), 1 if x.dtype == torch.bfloat16 else 0, rows, K,
+                                  codes.data_ptr(), sf_tiled.data_ptr(),
+                                  sf_rowmajor.data_ptr() if sf_rowmajor is not None else None,
+                                  _stream_handle(stream)), "nvfp4_quantize")
+    return codes, sf_tiled, sf_rowmajor
+
+
 def last_device_error(stream=None) -> int:
     return int(_abi.load().nvfp4_last_device_error(_stream_handle(stream)))
 

@@ -161,6 +161,30 @@ typedef struct SfRelayoutDesc {
 } SfRelayoutDesc;
 int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t stream);
 
+/* NVFP4 quantisation of a 16-bit float matrix into the GEMM's operand
+ * format (the step that produces A or B; the pages take quantised data as
+ * given, so this follows the generator of their "quantized" configuration:
+ * values quantised per 16-block to E2M1 with an absmax/6 scale rounded to
+ * E4M3FN).  For every 16-element block of a row:
+ *   scale = E4M3FN(absmax / 6)       round to nearest even, saturating at 448
+ *   code  = E2M1(x / scale)          round to nearest even, saturating at 6
+ * both on IEEE single-precision quotients rounded to nearest; a zero
+ * magnitude is stored as code 0 (no sign bit) and a block whose scale rounds
+ * to 0 (absmax < 6 * 2^-10, all zeros included) gets codes 0.
+ *  x           device, [rows][K] FP16 (x_is_bf16 = 0) or BF16 (x_is_bf16 =
+ *              1) elements, row stride K, finite values, 16-byte aligned.
+ *  codes       device, [rows][K/2] bytes, element 2i in the low nibble of
+ *              byte i (the GEMM's A / B layout), 16-byte aligned.
+ *  sf_tiled    device, nvfp4_sf_tiled_bytes(rows, K) bytes: the scales in
+ *              the tiled layout the GEMM reads (what nvfp4_sf_relayout
+ *              writes), padding rows zero; 16-byte aligned.
+ *  sf_rowmajor device [rows][K/16] bytes or NULL: the same scales row-major.
+ *  rows >= 0 (0 is a no-op), K % 64 == 0, rows, K <= 2^20.  Outputs must not
+ *  overlap the input.  Asynchronous on `stream`; returns NVFP4_OK or a
+ *  negative code (nothing launched). */
+int nvfp4_quantize(const void *x, int x_is_bf16, int rows, int K, void *codes, void *sf_tiled,
+                   void *sf_rowmajor, cudaStream_t stream);
+
 /* Bytes of the tiled scale buffer for a [rows][K/16] scale matrix:
  * ceil(rows / 128) * (K / 64) * 512; 0 for invalid sizes. */
 size_t nvfp4_sf_tiled_bytes(int rows, int K);
