@@ -558,3 +558,81 @@ int nvfp4_oracle_quantize(const uint16_t *x, int is_bf16, int rows, int K, uint8
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fused epilogue options of the grouped GEMM (an MoE layer's per-tensor    */
+/* scale, BF16 output and the SwiGLU of a gate/up projection), applied to   */
+/* the exact float64 sums.                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Round a double to bfloat16 (8 exponent bits, 8 significant bits) with
+ * round-to-nearest-even, returning the bit pattern: subnormals (multiples of
+ * 2^-133), overflow to +-inf, NaN as 0x7FC0. */
+uint16_t nvfp4_oracle_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0u;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    (void)frexp(a, &ex);            /* a = f * 2^ex, f in [0.5, 1) */
+    int qexp = ex - 8;
+    if (qexp < -133)
+        qexp = -133;
+    double r = ldexp(a, -qexp);
+    double fl = floor(r);
+    double diff = r - fl;
+    double n = fl;
+    if (diff > 0.5 || (diff == 0.5 && fmod(fl, 2.0) != 0.0))
+        n = fl + 1.0;
+    double v = ldexp(n, qexp);
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u);
+    if (v < ldexp(1.0, -126)) {
+        unsigned mant = (unsigned)ldexp(v, 133);
+        return (uint16_t)(sign | mant);
+    }
+    int e2;
+    double f = frexp(v, &e2);       /* v = f * 2^e2 */
+    unsigned efield = (unsigned)(e2 + 126);
+    unsigned mant = (unsigned)((f * 2.0 - 1.0) * 128.0);
+    return (uint16_t)(sign | (efield << 7) | mant);
+}
+
+/* SiLU in float64: x * sigmoid(x) = x / (1 + e^-x) */
+double nvfp4_oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+/* acc: the exact sums [M][N] of one group (float64).  Plain: out[m][n] =
+ * alpha * acc[m][n], [M][N].  SwiGLU (N % 256 == 0): the B rows come in
+ * 256-row blocks, 128 gate rows then the 128 up rows of the same outputs,
+ * and out[m][128 j + c] = silu(alpha * acc[m][256 j + c]) *
+ * (alpha * acc[m][256 j + 128 + c]), [M][N/2].  Rounded once, to BF16 if
+ * bf16 else FP16. */
+int nvfp4_oracle_epilogue(const double *acc, int M, int N, double alpha, int swiglu, int bf16,
+                          uint16_t *out)
+{
+    if (M < 0 || N <= 0 || !acc || !out || (swiglu && N % 256 != 0))
+        return -1;
+    const int nout = swiglu ? N / 2 : N;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < nout; ++n) {
+            double v;
+            if (swiglu) {
+                const int j = n / 128, c = n % 128;
+                const double g = alpha * acc[(size_t)m * N + 256 * j + c];
+                const double u = alpha * acc[(size_t)m * N + 256 * j + 128 + c];
+                v = nvfp4_oracle_silu(g) * u;
+            } else {
+                v = alpha * acc[(size_t)m * N + n];
+            }
+            out[(size_t)m * nout + n] = bf16 ? nvfp4_oracle_bf16_rne(v) : nvfp4_oracle_fp16_rne(v);
+        }
+    return 0;
+}

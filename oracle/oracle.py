@@ -96,6 +96,13 @@ class Oracle:
         L.nvfp4_oracle_sf_relayout.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int]
         L.nvfp4_oracle_sf_unrelayout.restype = ctypes.c_int
         L.nvfp4_oracle_sf_unrelayout.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int]
+        L.nvfp4_oracle_bf16_rne.restype = ctypes.c_uint16
+        L.nvfp4_oracle_bf16_rne.argtypes = [ctypes.c_double]
+        L.nvfp4_oracle_silu.restype = ctypes.c_double
+        L.nvfp4_oracle_silu.argtypes = [ctypes.c_double]
+        L.nvfp4_oracle_epilogue.restype = ctypes.c_int
+        L.nvfp4_oracle_epilogue.argtypes = [_f64p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                            ctypes.c_int, ctypes.c_int, _u16p]
         L.nvfp4_oracle_e4m3_rne.restype = ctypes.c_uint
         L.nvfp4_oracle_e4m3_rne.argtypes = [ctypes.c_float]
         L.nvfp4_oracle_e2m1_rne.restype = ctypes.c_uint
@@ -176,6 +183,30 @@ class Oracle:
         Returns a list of uint16 [M, N] arrays of FP16 bits."""
         return [self.gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, threads=threads)
                 for g in groups]
+
+    # fused epilogue -------------------------------------------------------------
+    def bf16_rne_bits(self, x: float) -> int:
+        return int(self.L.nvfp4_oracle_bf16_rne(float(x)))
+
+    def silu(self, x: float) -> float:
+        return float(self.L.nvfp4_oracle_silu(float(x)))
+
+    def epilogue(self, acc, alpha: float = 1.0, swiglu: bool = False, bf16: bool = False):
+        """From the exact float64 sums acc [M, N] of one group: alpha * acc,
+        or the SwiGLU of 128-row gate / up blocks ([M, N/2]); FP16 or BF16
+        bits (uint16)."""
+        acc = np.ascontiguousarray(acc, dtype=np.float64)
+        M, N = acc.shape
+        out = np.zeros((M, N // 2 if swiglu else N), dtype=np.uint16)
+        if M and self.L.nvfp4_oracle_epilogue(_p(acc, _f64p), M, N, float(alpha), int(swiglu),
+                                              int(bf16), _p(out, _u16p)) != 0:
+            raise ValueError("oracle epilogue failed")
+        return out
+
+    def gemm_ex(self, A, SFA, B, SFB, M, N, K, alpha=1.0, swiglu=False, bf16=False, threads=0):
+        """One group through the fused epilogue."""
+        _, acc = self.gemm(A, SFA, B, SFB, M, N, K, threads=threads, want_acc=True)
+        return self.epilogue(acc, alpha, swiglu, bf16)
 
     # quantisation ---------------------------------------------------------------
     def e4m3_rne(self, v: float) -> int:

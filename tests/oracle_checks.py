@@ -442,11 +442,64 @@ def check_quant_vs_float64_generator(o, seed=23):
     assert (np.abs(mag(a[diff]).astype(int) - mag(b[diff]).astype(int)) <= 1).all()
 
 
+# --- fused epilogue (per-tensor scale, BF16 output, SwiGLU) --------------
+
+def check_bf16_rounding(o, seed=31):
+    """Against PyTorch's float32 -> bfloat16 conversion (round to nearest
+    even) on float32 values: normals over the whole range, subnormals, exact
+    ties, overflow."""
+    rng = np.random.default_rng(seed)
+    vals = np.concatenate([
+        rng.standard_normal(3000) * np.exp(rng.uniform(-80, 80, 3000)),
+        rng.standard_normal(500) * 1e-39,
+        np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 3.3895e38, 3.39e38, 0.0]),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([o.bf16_rne_bits(float(v)) for v in vals], dtype=np.uint16)
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, [(float(vals[i]), hex(got[i]), hex(ref[i])) for i in bad[:5]]
+
+
+def check_silu(o, seed=32):
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([rng.standard_normal(200) * 20, [0.0, -800.0, 800.0]])
+    ref = torch.nn.functional.silu(torch.from_numpy(x)).numpy()
+    got = np.array([o.silu(float(v)) for v in x])
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-300), np.abs(got - ref).max()
+
+
+def check_epilogue_mapping(o):
+    """SwiGLU pairs output column 128 j + c with gate column 256 j + c and up
+    column 256 j + 128 + c; alpha scales both before the SiLU; the plain
+    epilogue scales every sum."""
+    M, N = 3, 512
+    acc = np.zeros((M, N))
+    acc[1, 256 + 5] = 2.0
+    acc[1, 256 + 128 + 5] = 3.0
+    acc[2, 7] = -4.0
+    acc[2, 128 + 7] = 0.5
+    alpha = 0.75
+    out = o.epilogue(acc, alpha=alpha, swiglu=True)
+    assert out.shape == (M, N // 2)
+    silu = lambda v: float(torch.nn.functional.silu(torch.tensor(v, dtype=torch.float64)))
+    exp = np.zeros((M, N // 2), dtype=np.float16)
+    exp[1, 128 + 5] = silu(alpha * 2.0) * alpha * 3.0
+    exp[2, 7] = silu(alpha * -4.0) * alpha * 0.5
+    assert np.array_equal(out.view(np.float16), exp), np.argwhere(out.view(np.float16) != exp)
+    out_b = o.epilogue(acc, alpha=alpha, swiglu=True, bf16=True)
+    exp_b = torch.from_numpy(exp.astype(np.float32)).to(torch.bfloat16)
+    got_b = torch.from_numpy(out_b.view(np.int16)).view(torch.bfloat16)
+    assert (got_b.float() - exp_b.float()).abs().max() <= 2 ** -7 * exp_b.float().abs().max()
+    plain = o.epilogue(acc, alpha=alpha).view(np.float16)
+    assert plain.shape == (M, N) and plain[1, 261] == np.float16(1.5) and plain[2, 135] == np.float16(0.375)
+    assert np.count_nonzero(plain) == 4
+
+
 ALL_CHECKS = [
     check_e2m1_table, check_e4m3_all_codes, check_fp16_rounding, check_brute_force_tiny,
     check_brute_force_grouped, check_fixed_point, check_single_nonzero,
     check_all_ones_power_of_two, check_zero_scales, check_nibble_order, check_scale_blocks,
     check_signs, check_row_and_column_split, check_transpose_symmetry, check_relayout,
     check_quant_e4m3_vs_torch, check_quant_e2m1_rounding, check_quant_blocks,
-    check_quant_vs_float64_generator,
+    check_quant_vs_float64_generator, check_bf16_rounding, check_silu, check_epilogue_mapping,
 ]

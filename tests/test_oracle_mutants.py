@@ -83,6 +83,20 @@ MUTANTS = {
         "        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {",
         "        const double d = fabs(x - nvfp4_oracle_e4m3fn(c));\n"
         "        if (nvfp4_oracle_e4m3fn(c) <= x) {"),
+    "swiglu_gate_up_swapped": (
+        "const double g = alpha * acc[(size_t)m * N + 256 * j + c];\n"
+        "                const double u = alpha * acc[(size_t)m * N + 256 * j + 128 + c];",
+        "const double g = alpha * acc[(size_t)m * N + 256 * j + 128 + c];\n"
+        "                const double u = alpha * acc[(size_t)m * N + 256 * j + c];"),
+    "swiglu_alpha_after_silu": (
+        "v = nvfp4_oracle_silu(g) * u;",
+        "v = nvfp4_oracle_silu(g / alpha) * alpha * u;"),
+    "bf16_mantissa_9_bits": (
+        "int qexp = ex - 8;\n    if (qexp < -133)",
+        "int qexp = ex - 9;\n    if (qexp < -133)"),
+    "silu_sign": (
+        "return x / (1.0 + exp(-x));",
+        "return x / (1.0 + exp(x));"),
     "fixed_point_shift": (
         "int shift = ea + eb - 2 + 20;",
         "int shift = ea + eb - 1 + 20;"),
