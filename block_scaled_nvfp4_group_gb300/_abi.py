@@ -33,6 +33,11 @@ class GroupDesc(ctypes.Structure):
                 ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int)]
 
 
+class GemmEpilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.POINTER(ctypes.c_float)), ("out_bf16", ctypes.c_int),
+                ("swiglu", ctypes.c_int)]
+
+
 class SfRelayoutDesc(ctypes.Structure):
     _fields_ = [("src", ctypes.c_void_p), ("dst", ctypes.c_void_p),
                 ("rows", ctypes.c_int), ("K", ctypes.c_int)]
@@ -43,6 +48,8 @@ SIGNATURES = {
     "nvfp4_group_gemm": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int, ctypes.c_void_p]),
     "nvfp4_group_gemm_noalloc": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
                                                 ctypes.c_void_p]),
+    "nvfp4_group_gemm_ex": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
+                                           ctypes.POINTER(GemmEpilogue), ctypes.c_void_p]),
     "nvfp4_group_gemm_plan": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int,
                                              ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_int)]),

@@ -43,6 +43,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
 
@@ -82,6 +83,10 @@ struct GemmParams {
     int b_policy;              // L2 policy of B / SFB loads: 0 normal, 1 first, 2 last
     int pf_stages;             // L2 prefetch distance for B, in stages ahead of the ring (0 = off)
     int debug_drop_stage;      // test hook: CTA 0's B loader never issues its first stage
+    // fused epilogue: C = alpha[g] * A B^T (or its SwiGLU), FP16 or BF16
+    float alpha[kMaxGroups];
+    int out_bf16;              // C elements: 0 FP16, 1 BF16
+    int swiglu;                // 1: every 256-column tile = 128 gate + 128 up columns, C is [M][N/2]
 };
 
 // Parameter block of a launch: the GEMM parameters and the 3-D maps of the
@@ -227,10 +232,74 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const Wai
     }
 }
 
-__device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_bits)
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16)
 {
-    __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    if (bf16) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&b);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// Epilogue, part 1: this thread's accumulator row of the tile (tensor-memory
+// lane `row_taddr`, columns [0, BN)) -> packed 16-bit output pairs in
+// registers, alpha applied; with SwiGLU, output column c of the tile is
+// silu(alpha * acc[c]) * alpha * acc[c + BN/2].  Column chunks at or past N
+// (input columns) are skipped.  Every lane of the warp takes part (the
+// tensor-memory loads are warp-collective).
+template <int BN, bool EPI_EX>
+__device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32_t row_taddr, int n0,
+                                              int N, uint32_t (&h)[BN / 2])
+{
+    if constexpr (!EPI_EX) {
+        // plain FP16
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+            if (n0 + c * 32 < N) {   // warp-uniform
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    h[c * 16 + i] = pack_out2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), false);
+            }
+        }
+        return;
+    }
+    const float alpha = p.alpha[g];
+    const bool bf = p.out_bf16 != 0;
+    if (!p.swiglu) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+            if (n0 + c * 32 < N) {   // warp-uniform
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    h[c * 16 + i] = pack_out2(alpha * __uint_as_float(v[2 * i]),
+                                              alpha * __uint_as_float(v[2 * i + 1]), bf);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {     // gate chunk c, up chunk c + BN/64
+            uint32_t gv[32], uv[32];
+            ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, gv);
+            ptx::tmem_ld_32x32b_x32(row_taddr + BN / 2 + c * 32, uv);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float o0 = silu(alpha * __uint_as_float(gv[2 * i])) * (alpha * __uint_as_float(uv[2 * i]));
+                const float o1 =
+                    silu(alpha * __uint_as_float(gv[2 * i + 1])) * (alpha * __uint_as_float(uv[2 * i + 1]));
+                h[c * 16 + i] = pack_out2(o0, o1, bf);
+            }
+        }
+    }
 }
 
 // stages of a tile: ceil(K / BK); the last one covers only K % BK when K is
@@ -385,7 +454,9 @@ __device__ __forceinline__ void prefetch_role(const KernelParams &kp, volatile u
     }
 }
 
-template <class Cfg>
+// EPI_EX: the fused epilogue options (alpha, BF16, SwiGLU) are compiled in;
+// the plain FP16 form keeps the default path's register budget.
+template <class Cfg, bool EPI_EX>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     nvfp4_group_gemm_kernel(const __grid_constant__ KernelParams kp)
 {
@@ -589,21 +660,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int N = p.N[tc.g];
             const int m0 = tc.bm * kBM + warp * 32;
             const int n0 = tc.bn * BN;
-            // 1. this thread's whole accumulator row -> FP16 pairs in registers
+            // 1. this thread's whole accumulator row -> 16-bit output pairs in
+            // registers
             uint32_t h[BN / 2];
-            if (m0 < M) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (n0 + c * 32 < N) {   // warp-uniform
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_tmem + acc * BN + c * 32, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[c * 16 + i] = pack_half2_rn(v[2 * i], v[2 * i + 1]);
-                    }
-                }
-            }
+            if (m0 < M)
+                epilogue_load<BN, EPI_EX>(p, tc.g, tmem_base + lane_tmem + acc * BN, n0, N, h);
             // 2. every lane's loads have completed (wait::ld): the accumulator
             // goes back to the MMA thread before the stores start, so the next
             // tile's MMAs overlap them
@@ -612,10 +673,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             if (lane == 0)
                 ptx::mbar_arrive(acce_bar(acc));
             // 3. swizzled shared staging + TMA tensor stores, EC columns each
+            const bool sw = EPI_EX && p.swiglu;
+            const int on0 = sw ? n0 / 2 : n0;     // output columns
+            const int oN = sw ? N / 2 : N;
+            const int ocols = sw ? BN / 2 : BN;
             if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
-                    if (n0 + c * EC < N) {   // warp-uniform
+                    if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform
                         // the store that last used this buffer must have
                         // finished reading it
                         if (lane == 0) {
@@ -641,7 +706,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         ptx::fence_proxy_async_shared();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmC[tc.g], buf, n0 + c * EC, m0);
+                            ptx::tma_store_2d(&p.tmC[tc.g], buf, on0 + c * EC, m0);
                             ptx::bulk_commit_group();
                         }
                         __syncwarp();

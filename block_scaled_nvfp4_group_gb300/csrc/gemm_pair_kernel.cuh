@@ -222,7 +222,7 @@ __device__ __forceinline__ void pair_prefetch(const KernelParams &kp, uint32_t r
     }
 }
 
-template <class Cfg>
+template <class Cfg, bool EPI_EX>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     nvfp4_group_gemm_pair_kernel(const __grid_constant__ KernelParams kp)
 {
@@ -402,27 +402,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int m0 = tc.bm * Cfg::kPairBM + (int)rank * kBM + warp * 32;
             const int n0 = tc.bn * BN;
             uint32_t h[BN / 2];
-            if (m0 < M) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (n0 + c * 32 < N) {   // warp-uniform
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_tmem + c * 32, v);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[c * 16 + i] = pack_half2_rn(v[2 * i], v[2 * i + 1]);
-                    }
-                }
-            }
+            if (m0 < M)
+                epilogue_load<BN, EPI_EX>(p, tc.g, tmem_base + lane_tmem, n0, N, h);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive_cluster(acce_leader);
+            const bool sw = EPI_EX && p.swiglu;
+            const int on0 = sw ? n0 / 2 : n0;     // output columns
+            const int oN = sw ? N / 2 : N;
+            const int ocols = sw ? BN / 2 : BN;
             if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
-                    if (n0 + c * EC < N) {   // warp-uniform
+                    if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform
                         if (lane == 0)
                             ptx::bulk_wait_group_read<0>();
                         __syncwarp();
@@ -437,7 +430,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         ptx::fence_proxy_async_shared();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmC[tc.g], stage_buf, n0 + c * EC, m0);
+                            ptx::tma_store_2d(&p.tmC[tc.g], stage_buf, on0 + c * EC, m0);
                             ptx::bulk_commit_group();
                         }
                         __syncwarp();

@@ -72,19 +72,21 @@ void make_launch_cfg(LaunchCfg &L, int grid, int threads, int smem, bool pair, c
 }
 
 template <class Cfg>
-cudaError_t launch_kind(const KernelParams &P, int grid, cudaStream_t s)
+cudaError_t launch_kind(const KernelParams &P, int grid, cudaStream_t s, bool ex)
 {
     LaunchCfg L;
     make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, false, s);
-    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg>, P);
+    return ex ? cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, true>, P)
+              : cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, false>, P);
 }
 
 template <class Cfg>
-cudaError_t launch_pair_kind(const KernelParams &P, int grid, cudaStream_t s)
+cudaError_t launch_pair_kind(const KernelParams &P, int grid, cudaStream_t s, bool ex)
 {
     LaunchCfg L;
     make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, true, s);
-    return cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_pair_kernel<Cfg>, P);
+    return ex ? cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_pair_kernel<Cfg, true>, P)
+              : cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_pair_kernel<Cfg, false>, P);
 }
 
 struct KindInfo {
@@ -98,8 +100,9 @@ struct KindInfo {
     int threads;
     int smem;
     bool pair;
-    const void *fn;
-    cudaError_t (*launch)(const KernelParams &, int, cudaStream_t);
+    const void *fn;      // plain FP16 epilogue
+    const void *fn_ex;   // fused epilogue options compiled in
+    cudaError_t (*launch)(const KernelParams &, int, cudaStream_t, bool);
 };
 
 template <class Cfg>
@@ -107,7 +110,8 @@ KindInfo make_kind()
 {
     return KindInfo{kBM, Cfg::BN, Cfg::BN, Cfg::kChunks, Cfg::kMmas, Cfg::BN / 128, Cfg::kEpiCols,
                     Cfg::kThreads, Cfg::kSmemBytes, false,
-                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg>), &launch_kind<Cfg>};
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, false>),
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, true>), &launch_kind<Cfg>};
 }
 
 template <class Cfg>
@@ -115,7 +119,8 @@ KindInfo make_pair_kind()
 {
     return KindInfo{Cfg::kPairBM, Cfg::BN, Cfg::BN / 2, 1, Cfg::kMmas, Cfg::kSfRb, Cfg::kEpiCols,
                     Cfg::kThreads, Cfg::kSmemBytes, true,
-                    reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg>),
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg, false>),
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg, true>),
                     &launch_pair_kind<Cfg>};
 }
 
@@ -142,7 +147,9 @@ int ensure_kernel_attributes(int dev, int kind)
     if (!g_attr_set[dev][kind]) {
         const KindInfo &ki = kind_info(kind);
         if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(ki.fn_ex, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) !=
+                cudaSuccess)
             return NVFP4_ERR_CUDA;
         if (ki.pair) {
             LaunchCfg L;
@@ -208,9 +215,14 @@ int validate_call(const GroupDesc *groups, int num_groups)
 // rounds of the grid and pairing does not add a round (large M, e.g. the
 // 4096^3 groups), never for the small-M MoE shapes.  NVFP4_GEMM_KIND
 // overrides the choice.
-int choose_kind(const GroupDesc *groups, int n, int sm_count)
+int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = false)
 {
-    const int forced = env_int("NVFP4_GEMM_KIND", -1);
+    const int forced_env = env_int("NVFP4_GEMM_KIND", -1);
+    // SwiGLU pairs the two 128-column halves of a 256-column tile
+    const int forced = (need_bn256 && forced_env >= 0 && forced_env < kNumKinds &&
+                        kind_info(forced_env).bn != 256)
+                           ? kKindWide
+                           : forced_env;
     bool all_n256 = true, all_n_ge256 = true;
     long long wide_tiles = 0, pair_tiles = 0;
     for (int i = 0; i < n; ++i)
@@ -283,8 +295,15 @@ int count_launches(const GroupDesc *groups, int num_groups, int bm, int bn)
 // live in a per-thread vector whose capacity is kept between calls.
 template <class ErrFn>
 int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
-                    int sm_count, int kind, ErrFn err_for_launch)
+                    int sm_count, int kind, ErrFn err_for_launch, const GemmEpilogue *epi = nullptr)
 {
+    const bool swiglu = epi && epi->swiglu;
+    const bool out_bf16 = epi && epi->out_bf16;
+    bool any_alpha = false;
+    if (epi && epi->alpha)
+        for (int i = 0; i < num_groups; ++i)
+            any_alpha = any_alpha || epi->alpha[i] != 1.0f;
+    const bool ex = swiglu || out_bf16 || any_alpha;
     static thread_local std::vector<KernelParams> plist;
     const KindInfo &ki = kind_info(kind);
     const int b_policy = choose_b_policy();
@@ -312,6 +331,8 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
             P.b_policy = b_policy;
             P.pf_stages = pf;
             P.debug_drop_stage = drop;
+            P.out_bf16 = out_bf16 ? 1 : 0;
+            P.swiglu = swiglu ? 1 : 0;
         }
         KernelParams &PP = plist.back();
         GemmParams &P = PP.g;
@@ -325,9 +346,12 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         if (rc == NVFP4_OK)
             rc = encode_map_sf(&PP.tmSFB[j], g.SFB, (uint64_t)g.N, (uint64_t)g.K, ki.sf_atoms,
                                ki.sfb_blocks);
+        const uint64_t n_out = swiglu ? (uint64_t)g.N / 2 : (uint64_t)g.N;
         if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P.tmC[j], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.C, (uint64_t)g.N,
-                               (uint64_t)g.M, (uint64_t)g.N * 2, ki.epi_cols, 32, c_swizzle);
+            rc = encode_map_2d(&P.tmC[j],
+                               out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                               g.C, n_out, (uint64_t)g.M, n_out * 2, ki.epi_cols, 32, c_swizzle);
+        P.alpha[j] = (epi && epi->alpha) ? epi->alpha[i] : 1.0f;
         P.M[j] = g.M;
         P.N[j] = g.N;
         P.kchunks[j] = g.K / kChunkK;
@@ -339,7 +363,7 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
     for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
         const KernelParams &P = plist[l];
         const int grid = grid_size(dev, kind, P.g.total_tiles, sm_count);
-        if (ki.launch(P, grid, stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        if (ki.launch(P, grid, stream, ex) != cudaSuccess || cudaGetLastError() != cudaSuccess)
             rc = NVFP4_ERR_CUDA;
     }
     return rc;
@@ -369,6 +393,35 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
     uint32_t *err = dev->err;
     return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; });
+}
+
+extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilogue *epi,
+                                   cudaStream_t stream)
+{
+    using namespace nvfp4;
+    int rc = validate_call(groups, num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    const bool swiglu = epi && epi->swiglu;
+    if (swiglu)
+        for (int i = 0; i < num_groups; ++i)
+            if (groups[i].M > 0 && groups[i].N % 256 != 0)
+                return NVFP4_ERR_INVALID_ARGUMENT;
+    DeviceState *dev = nullptr;
+    rc = current_device(&dev);
+    if (rc != NVFP4_OK)
+        return rc;
+    const int kind = choose_kind(groups, num_groups, dev->sm_count, swiglu);
+    if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+        return NVFP4_OK;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    rc = ensure_kernel_attributes(dev_id, kind);
+    if (rc != NVFP4_OK)
+        return rc;
+    uint32_t *err = dev->err;
+    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
+                           [err](int) { return err; }, epi);
 }
 
 extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind,

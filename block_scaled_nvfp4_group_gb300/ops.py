@@ -71,8 +71,9 @@ def sf_relayout_group(items, stream=None, descs=None) -> None:
                "nvfp4_sf_relayout_group")
 
 
-def make_group_descs(groups):
-    """groups: iterable of (A, B, SFA_tiled, SFB_tiled, C, M, N, K)."""
+def make_group_descs(groups, out_bf16: bool = False, swiglu: bool = False):
+    """groups: iterable of (A, B, SFA_tiled, SFB_tiled, C, M, N, K); C is
+    [M, N] float16, or as the fused epilogue writes it (bfloat16, [M, N/2])."""
     groups = list(groups)
     arr = (_abi.GroupDesc * len(groups))()
     for i, (A, B, SFA, SFB, C, M, N, K) in enumerate(groups):
@@ -81,8 +82,10 @@ def make_group_descs(groups):
             _check_u8(B, "B", N * K // 2)
             if SFA.numel() < sf_tiled_bytes(M, K) or SFB.numel() < sf_tiled_bytes(N, K):
                 raise ValueError("scale buffers too small")
-            if C.dtype != torch.float16 or C.numel() != M * N or not C.is_contiguous():
-                raise ValueError("C must be a contiguous float16 [M, N] tensor")
+            want = torch.bfloat16 if out_bf16 else torch.float16
+            n_out = N // 2 if swiglu else N
+            if C.dtype != want or C.numel() != M * n_out or not C.is_contiguous():
+                raise ValueError(f"C must be a contiguous {want} [M, {n_out}] tensor")
         arr[i] = _abi.GroupDesc(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
                                 C.data_ptr(), M, N, K)
     return arr
@@ -96,6 +99,25 @@ def group_gemm(groups, stream=None, descs=None) -> None:
     lib = _abi.load()
     arr = descs if descs is not None else make_group_descs(groups)
     _abi.check(lib.nvfp4_group_gemm(arr, len(arr), _stream_handle(stream)), "nvfp4_group_gemm")
+
+
+def group_gemm_ex(groups, alpha=None, out_bf16: bool = False, swiglu: bool = False, stream=None,
+                  descs=None) -> None:
+    """group_gemm with the fused epilogue (nvfp4_group_gemm_ex): per-group
+    scales `alpha` (sequence of floats or None), BF16 output, SwiGLU of
+    128-row gate / up blocks (C is then [M, N/2])."""
+    lib = _abi.load()
+    arr = descs if descs is not None else make_group_descs(groups, out_bf16=out_bf16, swiglu=swiglu)
+    epi = _abi.GemmEpilogue()
+    keep = None
+    if alpha is not None:
+        keep = (ctypes.c_float * len(arr))(*[float(a) for a in alpha])
+        epi.alpha = ctypes.cast(keep, ctypes.POINTER(ctypes.c_float))
+    epi.out_bf16 = 1 if out_bf16 else 0
+    epi.swiglu = 1 if swiglu else 0
+    _abi.check(lib.nvfp4_group_gemm_ex(arr, len(arr), ctypes.byref(epi), _stream_handle(stream)),
+               "nvfp4_group_gemm_ex")
+    del keep
 
 
 def group_gemm_plan(groups=None, descs=None):

@@ -77,6 +77,32 @@ typedef struct GroupDesc {
  * Returns NVFP4_OK or a negative code; nothing is launched on error. */
 int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStream_t stream);
 
+/* Fused epilogue options (an MoE layer's needs; the pages write plain FP16
+ * A.B^T): C_g = alpha[g] * A_g . B_g^T, optionally through the SwiGLU of a
+ * gate/up projection, stored as FP16 or BF16 (rounded to nearest even once,
+ * from the FP32 accumulator).
+ *  alpha     host array [num_groups] of per-group scales (the product of the
+ *            per-tensor global scales of A_g and B_g), or NULL for 1.
+ *  out_bf16  0: C elements FP16, 1: BF16.
+ *  swiglu    0: C_g is [M_g][N_g].  1: every N_g is a multiple of 256 and
+ *            the rows of B_g come in 256-row blocks, 128 gate rows followed
+ *            by the 128 up rows of the same outputs; C_g is [M_g][N_g/2] with
+ *            C[m][128 j + c] = silu(alpha g) * (alpha u), g = (A.B^T)[m][256 j
+ *            + c], u = (A.B^T)[m][256 j + 128 + c], silu(x) = x / (1 + e^-x)
+ *            in single precision. */
+typedef struct GemmEpilogue {
+    const float *alpha;
+    int out_bf16;
+    int swiglu;
+} GemmEpilogue;
+
+/* nvfp4_group_gemm with the fused epilogue options `epi` (NULL: plain FP16
+ * as nvfp4_group_gemm).  The ldc of C_g is its output width (N_g or N_g/2).
+ * Returns NVFP4_ERR_INVALID_ARGUMENT when swiglu is set and some non-empty
+ * group has N % 256 != 0. */
+int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilogue *epi,
+                        cudaStream_t stream);
+
 /* Kernel configurations of the grouped GEMM (chosen per call from the
  * shapes; the environment variable NVFP4_GEMM_KIND forces one):
  *  STREAM  128 x 128 tiles, 512-K stages (any N)

@@ -35,6 +35,24 @@ def compare_fp16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
                              f"oracle {r[tuple(idx[0])]}")
 
 
+BF16_RTOL = 2.0 ** -7   # one BF16 ulp: the FP32 sum may round to the neighbour of the exact sum's BF16
+
+
+def compare_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
+    """Elementwise |gpu - oracle| <= 2^-7 |oracle| + 1e-2 on BF16 outputs."""
+    g = (got_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = (ref_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    fin = np.isfinite(r)
+    assert np.array_equal(np.isfinite(g), fin), f"{what}: non-finite pattern differs"
+    err = np.abs(g[fin] - r[fin])
+    bad = err > BF16_RTOL * np.abs(r[fin]) + ATOL
+    if bad.any():
+        idx = np.argwhere(fin)[np.flatnonzero(bad)[:5]]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} out of tolerance; first at "
+                             f"{idx.tolist()}: gpu {g[tuple(idx[0])]} oracle {r[tuple(idx[0])]}")
+
+
 KINDS = {"stream": 0, "wide": 1, "compute": 2, "wide512": 3, "wide_p2": 4, "wide_p4": 5,
          "pair": 6}
 
