@@ -9,11 +9,15 @@
 // the 32 x 16-byte shape of one tcgen05.cp 32x128b.warpx4 (474067,
 // tcgen05_cp_nvfp4).  Rows past `rows` in the last block become zero.
 //
-// The relayout is a byte permutation, HBM-bound: one CTA moves up to four
-// 128-row x 64-scale blocks (32 KiB in, 32 KiB out) through shared memory,
-// with 16-byte loads along source rows (all issued before the first wait) and
-// 16-byte stores along atom rows, both coalesced.  Algorithmic traffic: rows * K/16 bytes read, the tiled size
-// written.
+// The relayout is a byte permutation, HBM-bound.  Persistent CTAs (four per
+// SM) walk the work items (one 128-row block x 64 scale columns = 16 atoms,
+// 8 KiB) round robin; each keeps four items in flight: a 2-D TMA load brings
+// the row-major tile into shared memory (rows past `rows` and columns past
+// K/16 read as zero), 256 threads transpose it (each 16-byte atom row is
+// four 4-byte words from rows q, q+32, q+64, q+96; the lane order makes the
+// shared-memory reads conflict-free) and write 32-byte runs of atoms to
+// global memory while the next tiles load.  Algorithmic traffic: rows * K/16
+// bytes read, the tiled size written.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -26,93 +30,133 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kMaxDescs = 64;     // relayouts per launch (param block)
-constexpr int kChunkScales = 64;  // scale columns per CTA = 16 atoms
-constexpr int kRowBlocks = 4;     // 128-row blocks per CTA
+constexpr int kChunkScales = 64;  // scale columns per item = 16 atoms
 constexpr int kThreads = 256;
-constexpr int kPitchWords = 17;   // 64 bytes + 4 bytes pad per staged row
+constexpr int kBufs = 4;          // items in flight per CTA
+constexpr int kTileBytes = 128 * kChunkScales;
+constexpr int kCtasPerSm = 4;
 constexpr int kMaxDim = 1 << 20;
 constexpr int kMaxCount = 4096;
-// 16-byte loads per thread: kRowBlocks * 128 rows * 4 vectors / kThreads
-constexpr int kLoadsPerThread = kRowBlocks * 128 * (kChunkScales / 16) / kThreads;
 
 struct RelayoutParams {
-    const uint8_t *src[kMaxDescs];
+    CUtensorMap tm[kMaxDescs];   // uint8 {K/16, rows}, box {64, 128}, no swizzle
     uint8_t *dst[kMaxDescs];
-    int rows[kMaxDescs];
-    int kcols[kMaxDescs];     // K / 16 scale columns per row
-    int chunks[kMaxDescs];    // ceil(kcols / 64)
-    int item_end[kMaxDescs];  // inclusive prefix sum of row-block groups * chunks
+    int kcols[kMaxDescs];        // K / 16 scale columns per row
+    int chunks[kMaxDescs];       // ceil(kcols / 64)
+    int item_end[kMaxDescs];     // inclusive prefix sum of row blocks * chunks
     int count;
+    int total_items;
+    uint32_t *err;
+    unsigned long long timeout_ns;
 };
 
-// One CTA: kRowBlocks consecutive 128-row blocks x one 64-column chunk.
-// Every thread issues all of its 16-byte loads before the first shared store,
-// so a CTA keeps up to 32 KiB of reads in flight.
+__device__ __forceinline__ void decode_item(const RelayoutParams &p, int item, int &d, int &rb, int &cc)
+{
+    d = 0;
+    while (item >= p.item_end[d])
+        ++d;
+    const int local = item - (d > 0 ? p.item_end[d - 1] : 0);
+    rb = local / p.chunks[d];
+    cc = local % p.chunks[d];
+}
+
 __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
 {
-    __shared__ uint32_t tile[kRowBlocks * 128 * kPitchWords];
+    __shared__ __align__(128) uint8_t tile[kBufs][kTileBytes];
+    __shared__ __align__(8) uint64_t bars[kBufs];
+    __shared__ int ok_flag;
     // programmatic launch: start early, but read and write global memory only
     // once the previous kernel in the stream is done
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    const int item = blockIdx.x;
-    int d = 0;
-    while (item >= p.item_end[d])
-        ++d;
-    const int local = item - (d > 0 ? p.item_end[d - 1] : 0);
-    const int chunks = p.chunks[d];
-    const int rbg = local / chunks;             // group of kRowBlocks row blocks
-    const int kc = local % chunks;
-    const int kcols = p.kcols[d];
-    const int rows = p.rows[d];
-    const int rblocks = (rows + 127) / 128;
-    const int nrb = min(kRowBlocks, rblocks - rbg * kRowBlocks);   // row blocks here
-    const int width = min(kChunkScales, kcols - kc * kChunkScales);  // multiple of 16
-    const int nvec = width / 16;
-    const int row0 = rbg * kRowBlocks * 128;
-
-    // loads: rows [row0, row0 + nrb*128) x `width` bytes, zero past `rows`
-    const uint8_t *src = p.src[d] + (size_t)kc * kChunkScales;
-    const int nload = nrb * 128 * nvec;
-    uint4 x[kLoadsPerThread];
-#pragma unroll
-    for (int i = 0; i < kLoadsPerThread; ++i) {
-        const int v = threadIdx.x + i * kThreads;
-        const int r = v / nvec, c = v % nvec;
-        x[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (v < nload && row0 + r < rows)
-            x[i] = __ldcs(reinterpret_cast<const uint4 *>(src + (size_t)(row0 + r) * kcols) + c);
-    }
-#pragma unroll
-    for (int i = 0; i < kLoadsPerThread; ++i) {
-        const int v = threadIdx.x + i * kThreads;
-        if (v < nload) {
-            const int r = v / nvec, c = v % nvec;
-            uint32_t *t = tile + r * kPitchWords + c * 4;
-            t[0] = x[i].x;
-            t[1] = x[i].y;
-            t[2] = x[i].z;
-            t[3] = x[i].w;
-        }
+    const uint32_t bar0 = ptx::smem_addr(&bars[0]);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kBufs; ++b)
+            ptx::mbar_init(bar0 + 8u * b, 1);
+        ptx::fence_mbar_init();
     }
     __syncthreads();
+    const uint64_t pol = ptx::policy_evict_first();
+    uint32_t inflight = 0, inflight_parity = 0;    // thread 0's issued loads
+    auto issue = [&](int k) {
+        const int item = (int)blockIdx.x + k * (int)gridDim.x;
+        if (item >= p.total_items)
+            return;
+        int d, rb, cc;
+        decode_item(p, item, d, rb, cc);
+        const int b = k % kBufs;
+        const uint32_t bar = bar0 + 8u * b;
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes);
+        ptx::tma_load_2d(ptx::smem_addr(&tile[b][0]), &p.tm[d], cc * kChunkScales, rb * 128, bar, pol);
+        inflight |= 1u << b;
+        inflight_parity = (inflight_parity & ~(1u << b)) | ((uint32_t)((k / kBufs) & 1) << b);
+    };
+    if (threadIdx.x == 0)
+        for (int k = 0; k < kBufs; ++k)
+            issue(k);
 
-    // atom a of row block rr: 16-byte row q holds rows q, q+32, q+64, q+96
-    const int natoms = width / 4;
-    const int nout = nrb * natoms * 32;
-    for (int o = threadIdx.x; o < nout; o += kThreads) {
-        const int rr = o / (natoms * 32);
-        const int a = (o >> 5) % natoms, q = o & 31;
-        const uint32_t *t = tile + rr * 128 * kPitchWords;
-        uint4 y;
-        y.x = t[(q)*kPitchWords + a];
-        y.y = t[(q + 32) * kPitchWords + a];
-        y.z = t[(q + 64) * kPitchWords + a];
-        y.w = t[(q + 96) * kPitchWords + a];
-        const size_t rb = (size_t)rbg * kRowBlocks + rr;
-        uint8_t *dst = p.dst[d] + (rb * (kcols / 4) + (size_t)kc * (kChunkScales / 4) + a) * 512;
-        *reinterpret_cast<uint4 *>(dst + q * 16) = y;
+    for (int k = 0;; ++k) {
+        const int item = (int)blockIdx.x + k * (int)gridDim.x;
+        if (item >= p.total_items)
+            break;
+        const int b = k % kBufs;
+        if (threadIdx.x == 0) {
+            // bounded wait for the tile; on expiry record it and stop (uniformly)
+            const uint32_t bar = bar0 + 8u * b, par = (uint32_t)((k / kBufs) & 1);
+            const uint64_t t0 = ptx::globaltimer_ns();
+            int ok = 1;
+            while (!ptx::mbar_try_wait(bar, par)) {
+                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+                    atomicOr(p.err, 1u);
+                    ok = 0;
+                    break;
+                }
+            }
+            if (ok)
+                inflight &= ~(1u << b);
+            ok_flag = ok;
+        }
+        __syncthreads();
+        if (!ok_flag)
+            break;
+        int d, rb, cc;
+        decode_item(p, item, d, rb, cc);
+        const int kcols = p.kcols[d];
+        const int natoms = min(16, (kcols - cc * kChunkScales) / 4);
+        const uint8_t *t = tile[b];
+        uint8_t *out = p.dst[d] + ((size_t)rb * (kcols / 4) + (size_t)cc * 16) * 512;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int idx = threadIdx.x + kThreads * pass;     // 0..511
+            const int a = idx & 15;                            // atom
+            const int l = 2 * (idx >> 5) + ((idx >> 4) & 1);   // 16-byte row of the atom
+            if (a < natoms) {
+                uint4 y;
+                y.x = *reinterpret_cast<const uint32_t *>(t + (l)*kChunkScales + 4 * a);
+                y.y = *reinterpret_cast<const uint32_t *>(t + (l + 32) * kChunkScales + 4 * a);
+                y.z = *reinterpret_cast<const uint32_t *>(t + (l + 64) * kChunkScales + 4 * a);
+                y.w = *reinterpret_cast<const uint32_t *>(t + (l + 96) * kChunkScales + 4 * a);
+                *reinterpret_cast<uint4 *>(out + (size_t)a * 512 + l * 16) = y;
+            }
+        }
+        __syncthreads();    // tile[b] fully read before it is reloaded
+        if (threadIdx.x == 0)
+            issue(k + kBufs);
+    }
+    // loads issued but not consumed (after an expired wait) still write this
+    // CTA's shared memory: wait for them (bounded) before exiting
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kBufs; ++b) {
+            if (!(inflight & (1u << b)))
+                continue;
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar0 + 8u * b, (inflight_parity >> b) & 1u))
+                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+                    atomicOr(p.err, 2u);
+                    break;
+                }
+        }
     }
 }
 
@@ -158,12 +202,16 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
     if (rc != NVFP4_OK)
         return rc;
 
-    RelayoutParams P{};
+    static thread_local RelayoutParams P;
     auto launch = [&]() -> int {
         if (P.count == 0)
             return NVFP4_OK;
+        P.total_items = P.item_end[P.count - 1];
+        P.err = dev->err;
+        P.timeout_ns = wait_timeout_ns();
+        const int max_ctas = dev->sm_count * kCtasPerSm;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(P.item_end[P.count - 1]);
+        cfg.gridDim = dim3(P.total_items < max_ctas ? P.total_items : max_ctas);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
@@ -185,7 +233,7 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
         const int kcols = d.K / 16;
         const int chunks = (kcols + kChunkScales - 1) / kChunkScales;
         const int rblocks = (d.rows + 127) / 128;
-        const long long n = (long long)((rblocks + kRowBlocks - 1) / kRowBlocks) * chunks;
+        const long long n = (long long)rblocks * chunks;
         if (P.count == kMaxDescs || (long long)items + n > (1ll << 30)) {
             rc = launch();
             if (rc != NVFP4_OK)
@@ -193,10 +241,13 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
             P.count = 0;
             items = 0;
         }
-        const int j = P.count++;
-        P.src[j] = static_cast<const uint8_t *>(d.src);
+        const int j = P.count;
+        rc = encode_map_2d(&P.tm[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, d.src, (uint64_t)kcols,
+                           (uint64_t)d.rows, (uint64_t)kcols, kChunkScales, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != NVFP4_OK)
+            return rc;
+        P.count = j + 1;
         P.dst[j] = static_cast<uint8_t *>(d.dst);
-        P.rows[j] = d.rows;
         P.kcols[j] = kcols;
         P.chunks[j] = chunks;
         items += (int)n;
