@@ -677,20 +677,26 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int on0 = sw ? n0 / 2 : n0;     // output columns
             const int oN = sw ? N / 2 : N;
             const int ocols = sw ? BN / 2 : BN;
+            // the CTA's last tile: every MMA has completed and no load is
+            // left, so the operand ring is free -- each chunk gets its own
+            // staging buffer there and the stores go out back to back
+            const bool last_tile = t + (int)gridDim.x >= total;
+            const uint32_t ring_buf = base + (uint32_t)(warp * (BN / EC)) * Cfg::kEpiBufBytes;
             if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
                     if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform
                         // the store that last used this buffer must have
                         // finished reading it
-                        if (lane == 0) {
+                        if (lane == 0 && !last_tile) {
                             if constexpr (Cfg::kEpiBufs == 2)
                                 ptx::bulk_wait_group_read<1>();
                             else
                                 ptx::bulk_wait_group_read<0>();
                         }
                         __syncwarp();
-                        const uint32_t buf = stage_buf + sbuf * Cfg::kEpiBufBytes;
+                        const uint32_t buf =
+                            last_tile ? ring_buf + c * Cfg::kEpiBufBytes : stage_buf + sbuf * Cfg::kEpiBufBytes;
                         // one row of EC halves per lane; 16-byte chunk q of row
                         // r sits at chunk q ^ (swizzle phase of r), the pattern
                         // of the C tensor map's EC*2-byte swizzle

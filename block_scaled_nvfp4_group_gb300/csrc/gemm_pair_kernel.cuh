@@ -412,15 +412,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int on0 = sw ? n0 / 2 : n0;     // output columns
             const int oN = sw ? N / 2 : N;
             const int ocols = sw ? BN / 2 : BN;
+            // the CTA's last tile: every MMA has completed and no load is
+            // left, so the operand ring is free -- each chunk gets its own
+            // staging buffer there and the stores go out back to back
+            const bool last_tile = t + npairs >= total;
+            const uint32_t ring_buf = base + (uint32_t)(warp * (BN / EC)) * Cfg::kEpiBufBytes;
             if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
                     if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform
-                        if (lane == 0)
+                        if (lane == 0 && !last_tile)
                             ptx::bulk_wait_group_read<0>();
                         __syncwarp();
+                        const uint32_t buf = last_tile ? ring_buf + c * Cfg::kEpiBufBytes : stage_buf;
                         constexpr int kQ = EC / 8;
-                        const uint32_t row = stage_buf + lane * (EC * 2);
+                        const uint32_t row = buf + lane * (EC * 2);
                         const int phase_r = (EC == 64) ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
                         for (int q = 0; q < kQ; ++q)
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                         ptx::fence_proxy_async_shared();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmC[tc.g], stage_buf, on0 + c * EC, m0);
+                            ptx::tma_store_2d(&p.tmC[tc.g], buf, on0 + c * EC, m0);
                             ptx::bulk_commit_group();
                         }
                         __syncwarp();
