@@ -29,16 +29,40 @@ class DeviceProblem:
         self.shapes = [(g.M, g.N, g.K) for g in groups]
         self.A, self.B, self.SFA, self.SFB = [], [], [], []
         self.SFA_t, self.SFB_t, self.C = [], [], []
+        # every input in one device buffer and every output in another (views
+        # at 256-byte offsets), so a batch moves host <-> device in one copy
+        # each way
+        in_sizes = []
         for g in groups:
-            self.A.append(_dev(g.A, self.device))
-            self.B.append(_dev(g.B, self.device))
-            self.SFA.append(_dev(g.SFA, self.device))
-            self.SFB.append(_dev(g.SFB, self.device))
+            in_sizes += [g.A.size, g.B.size, g.SFA.size, g.SFB.size]
+        offs, total = [], 0
+        for n in in_sizes:
+            offs.append(total)
+            total += (n + 255) // 256 * 256
+        self.inputs = torch.zeros(max(total, 256), dtype=torch.uint8, device=self.device)
+        host = np.zeros(max(total, 256), dtype=np.uint8)
+        out_offs, out_total = [], 0
+        for (M, N, K) in self.shapes:
+            out_offs.append(out_total)
+            out_total += (M * N * 2 + 255) // 256 * 256
+        self.outputs = torch.empty(max(out_total, 256), dtype=torch.uint8, device=self.device)
+        for i, g in enumerate(groups):
+            views = []
+            for j, arr in enumerate((g.A, g.B, g.SFA, g.SFB)):
+                o = offs[4 * i + j]
+                host[o:o + arr.size] = np.ascontiguousarray(arr).reshape(-1)
+                views.append(self.inputs[o:o + arr.size])
+            self.A.append(views[0])
+            self.B.append(views[1])
+            self.SFA.append(views[2])
+            self.SFB.append(views[3])
             self.SFA_t.append(torch.zeros(max(ops.sf_tiled_bytes(g.M, g.K), 16), dtype=torch.uint8,
                                           device=self.device))
             self.SFB_t.append(torch.zeros(max(ops.sf_tiled_bytes(g.N, g.K), 16), dtype=torch.uint8,
                                           device=self.device))
-            self.C.append(torch.empty((g.M, g.N), dtype=torch.float16, device=self.device))
+            o = out_offs[i]
+            self.C.append(self.outputs[o:o + g.M * g.N * 2].view(torch.float16).view(g.M, g.N))
+        self.inputs.copy_(torch.from_numpy(host))
         self.relayout_items = []
         for i, (M, N, K) in enumerate(self.shapes):
             if M > 0:   # an empty group is skipped by the GEMM as well
