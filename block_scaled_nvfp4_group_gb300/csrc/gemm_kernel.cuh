@@ -71,6 +71,12 @@ struct GemmParams {
     CUtensorMap tmA[kMaxGroups];  // uint8 {128 B, M, K/256}, box {128, 128, BK/256}, 128B swizzle
     CUtensorMap tmB[kMaxGroups];  // uint8 {128 B, N, K/256}, box {128, BN, BK/256}
     CUtensorMap tmC[kMaxGroups];  // fp16 [M][N], box EPI_COLS x 32, swizzle = EPI_COLS * 2 B
+    // C as 64-column blocks, {64, M, N/64} with strides {2N, 128} bytes, box
+    // {64, 32, tile columns / 64}, 128-byte swizzle: the whole 32-row slab of
+    // a tile in one store (used for a CTA's last tile; c_wide[g] = 0 when N
+    // is not a multiple of 64)
+    CUtensorMap tmCw[kMaxGroups];
+    int c_wide[kMaxGroups];
     int M[kMaxGroups];
     int N[kMaxGroups];
     int kchunks[kMaxGroups];   // K / 256
@@ -98,6 +104,7 @@ struct KernelParams {
     CUtensorMap tmSFA[kMaxGroups];  // box {128, BK/64, 1}
     CUtensorMap tmSFB[kMaxGroups];  // box {128, BK/64, BN/128} (BN/2 per CTA of a pair: 128 rows each)
 };
+static_assert(sizeof(KernelParams) <= 32764, "kernel parameter block over 32 KiB");
 
 // BN: tile width; BK: K elements per stage (256 or 512); STAGES: ring depth;
 // EPI_COLS: columns per epilogue store (32 or 64); EPI_BUFS: staging
@@ -134,6 +141,7 @@ struct GemmConfig {
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag, MMA progress
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
+    static_assert(kStages * kStageBytes >= 4 * (BN / 64) * 4096, "ring too small for the last tile's slabs");
     // tensor memory: accumulators, then one scale region per ring slot
     // (SFA atoms, then SFB atoms): the copies for stage q+1 never write the
     // columns the MMAs of stage q read, so they need not wait for them
@@ -250,6 +258,35 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x));
 // silu(alpha * acc[c]) * alpha * acc[c + BN/2].  Column chunks at or past N
 // (input columns) are skipped.  Every lane of the warp takes part (the
 // tensor-memory loads are warp-collective).
+// Epilogue, part 2 for a CTA's last tile (the operand ring is idle): the
+// warp's 32 rows x `ocols` output columns as 64-column blocks of 32 rows x
+// 128 bytes with the 128-byte swizzle (16-byte chunk q of row r at q ^ (r % 8):
+// conflict-free), then a single 3-D tensor store for the warp -- one TMA
+// operation instead of one per EC columns.  `buf` is 1024-byte aligned and
+// holds BN / 64 blocks of 4 KiB.
+template <int BN>
+__device__ __forceinline__ void store_slab_wide(const CUtensorMap *tm, uint32_t buf, int lane, int on0, int oN,
+                                                int ocols, int m0, const uint32_t (&h)[BN / 2])
+{
+#pragma unroll
+    for (int ch = 0; ch < BN / 64; ++ch) {
+        if (ch * 64 < ocols && on0 + ch * 64 < oN) {   // warp-uniform
+            const uint32_t row = buf + (uint32_t)ch * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                ptx::st_shared_v4(row + ((q ^ (lane & 7)) << 4), h[ch * 32 + 4 * q], h[ch * 32 + 4 * q + 1],
+                                  h[ch * 32 + 4 * q + 2], h[ch * 32 + 4 * q + 3]);
+        }
+    }
+    ptx::fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_3d(tm, buf, 0, m0, on0 / 64);
+        ptx::bulk_commit_group();
+    }
+    __syncwarp();
+}
+
 template <int BN, bool EPI_EX>
 __device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32_t row_taddr, int n0,
                                               int N, uint32_t (&h)[BN / 2])
@@ -682,7 +719,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // staging buffer there and the stores go out back to back
             const bool last_tile = t + (int)gridDim.x >= total;
             const uint32_t ring_buf = base + (uint32_t)(warp * (BN / EC)) * Cfg::kEpiBufBytes;
-            if (m0 < M) {
+            if (m0 < M && last_tile && p.c_wide[tc.g]) {
+                store_slab_wide<BN>(&p.tmCw[tc.g], base + (uint32_t)(warp * (BN / 64)) * 4096u, lane, on0, oN,
+                                    ocols, m0, h);
+            } else if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
                     if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform

@@ -75,6 +75,7 @@ struct PairConfig {
     static constexpr int kSlotOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag, B progress
     static constexpr int kSmemBytes = kSlotOff + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "exceeds 227 KiB of shared memory");
+    static_assert(kStages * kStageBytes >= 4 * (BN / 64) * 4096, "ring too small for the last tile's slabs");
     static constexpr int kMmaWarpP = 4;
     static constexpr int kSfWarpP = 5;
     static constexpr int kFirstLoader = 6;   // A, B, A scales, B scales
@@ -417,7 +418,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // staging buffer there and the stores go out back to back
             const bool last_tile = t + npairs >= total;
             const uint32_t ring_buf = base + (uint32_t)(warp * (BN / EC)) * Cfg::kEpiBufBytes;
-            if (m0 < M) {
+            if (m0 < M && last_tile && p.c_wide[tc.g]) {
+                store_slab_wide<BN>(&p.tmCw[tc.g], base + (uint32_t)(warp * (BN / 64)) * 4096u, lane, on0, oN,
+                                    ocols, m0, h);
+            } else if (m0 < M) {
 #pragma unroll
                 for (int c = 0; c < BN / EC; ++c) {
                     if (c * EC < ocols && on0 + c * EC < oN) {   // warp-uniform

@@ -347,10 +347,19 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
             rc = encode_map_sf(&PP.tmSFB[j], g.SFB, (uint64_t)g.N, (uint64_t)g.K, ki.sf_atoms,
                                ki.sfb_blocks);
         const uint64_t n_out = swiglu ? (uint64_t)g.N / 2 : (uint64_t)g.N;
+        const CUtensorMapDataType c_type =
+            out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         if (rc == NVFP4_OK)
-            rc = encode_map_2d(&P.tmC[j],
-                               out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                               g.C, n_out, (uint64_t)g.M, n_out * 2, ki.epi_cols, 32, c_swizzle);
+            rc = encode_map_2d(&P.tmC[j], c_type, g.C, n_out, (uint64_t)g.M, n_out * 2, ki.epi_cols, 32,
+                               c_swizzle);
+        // the single-store form of a CTA's last tile, where C's rows are
+        // whole 64-column blocks; otherwise (or if the driver declines the
+        // map) the last tile takes the per-chunk stores
+        P.c_wide[j] = 0;
+        if (rc == NVFP4_OK && n_out % 64 == 0 &&
+            encode_map_c_wide(&P.tmCw[j], c_type, g.C, (uint64_t)g.M, n_out,
+                              (uint32_t)((swiglu ? ki.bn / 2 : ki.bn) / 64)) == NVFP4_OK)
+            P.c_wide[j] = 1;
         P.alpha[j] = (epi && epi->alpha) ? epi->alpha[i] : 1.0f;
         P.M[j] = g.M;
         P.N[j] = g.N;

@@ -171,6 +171,14 @@ int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, 
     return encode_map(out, key);
 }
 
+int encode_map_c_wide(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t rows,
+                      uint64_t cols, uint32_t box_blocks)
+{
+    const MapKey key{ptr, 64, rows, cols / 64, cols * 2, 128, 64, 32, box_blocks, 3, (int)dtype,
+                     (int)CU_TENSOR_MAP_SWIZZLE_128B};
+    return encode_map(out, key);
+}
+
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 int debug_drop_stage() { return g_debug_drop.load(std::memory_order_relaxed); }
 int b_policy_override() { return read_env_int("NVFP4_B_POLICY", -1); }

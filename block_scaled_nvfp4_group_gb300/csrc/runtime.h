@@ -41,6 +41,11 @@ int encode_map_operand(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_
 // (zeros past the last atom or row block).
 int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_atoms,
                   uint32_t box_blocks);
+// 16-bit C [rows][cols] (cols a multiple of 64) seen as 64-column blocks:
+// {64, rows, cols / 64} with strides {2 cols, 128} bytes, box {64, 32,
+// box_blocks}, 128-byte swizzle (one tile's 32-row slab per store)
+int encode_map_c_wide(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t rows,
+                      uint64_t cols, uint32_t box_blocks);
 
 unsigned long long wait_timeout_ns();
 int debug_drop_stage();
