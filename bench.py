@@ -281,9 +281,16 @@ def run_ours(args):
 
     # The step (and each of its two launches alone) captured as CUDA graphs:
     # replays are back to back on the GPU, free of Python/host launch gaps.
+    # Captured on a stream that has run the step before: a stream's first
+    # stream-K GEMM allocates its scratch, which cannot happen during capture.
+    cap_stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(cap_stream):
+        prob.step()
+    torch.cuda.synchronize()
+
     def capture(fn):
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        with torch.cuda.graph(g, stream=cap_stream):
             fn()
         return g
     g_step = capture(prob.step)

@@ -65,7 +65,14 @@ constexpr int kSmemLimit = 232448; // 227 KiB per CTA
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrDrainTimeout = 2u;
 
-enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleDrain = 4, kRoleSf = 5 };
+enum : uint32_t {
+    kRoleProducer = 1,
+    kRoleMma = 2,
+    kRoleEpilogue = 3,
+    kRoleDrain = 4,
+    kRoleSf = 5,
+    kRoleStreamK = 6   // an epilogue warp waiting for another CTA's partial sum
+};
 
 struct GemmParams {
     CUtensorMap tmA[kMaxGroups];  // uint8 {128 B, M, K/256}, box {128, 128, BK/256}, 128B swizzle
@@ -93,6 +100,14 @@ struct GemmParams {
     float alpha[kMaxGroups];
     int out_bf16;              // C elements: 0 FP16, 1 BF16
     int swiglu;                // 1: every 256-column tile = 128 gate + 128 up columns, C is [M][N/2]
+    // stream-K launches: the flat sequence of (tile, k-stage) units, tiles in
+    // list order, is cut into gridDim.x contiguous ranges, CTA c taking units
+    // [c U / G, (c + 1) U / G) with U = units_total
+    int units_total;
+    int unit_end[kMaxGroups];  // inclusive prefix sum of tiles x stages
+    float *sk_ws;              // per CTA one partial accumulator, 128 x BN FP32
+    uint32_t *sk_flags;        // per CTA and epilogue warp: epoch of its last partial
+    uint32_t *sk_epoch;        // [0] epoch of the launch, [1] CTAs finished
 };
 
 // Parameter block of a launch: the GEMM parameters and the 3-D maps of the
@@ -240,6 +255,68 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const Wai
     }
 }
 
+// stream-K: bounded wait until another CTA has published `value` in `flag`
+// (release / acquire at GPU scope); false when it expired (error word and
+// abort flag set) or another role aborted
+__device__ __noinline__ bool wait_flag_bounded(const uint32_t *flag, uint32_t value, const WaitCtx &w)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+        if (ptx::ld_acquire_gpu(flag) == value)
+            return true;
+        if (*w.abort)
+            return false;
+        if (ptx::globaltimer_ns() - t0 > w.timeout_ns) {
+            *w.abort = 1u;
+            atomicOr(w.err, kErrTimeout);
+            atomicCAS(w.err + 1, 0u, (blockIdx.x << 4) | kRoleStreamK);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+// Stream-K partial accumulators: CTA c's slot holds 128 rows x BN FP32 values
+// with element (r, x) in float4 number (x / 4) * 128 + r, so a warp's 32 rows
+// of four columns are 512 contiguous bytes on both sides.
+template <int BN>
+__device__ __forceinline__ void store_partial(float *ws, uint32_t row_taddr, int n0, int N, int row)
+{
+    float4 *d4 = reinterpret_cast<float4 *>(ws + (size_t)blockIdx.x * (BN * 128)) + row;
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+        if (n0 + c * 32 < N) {   // warp-uniform
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                __stcg(d4 + (c * 8 + i) * 128,
+                       make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+    }
+}
+
+// adds the partial sums of CTAs [h0, h1) to 32 accumulator columns (chunk
+// `chunk` of 32) of this thread's row
+template <int BN>
+__device__ __forceinline__ void add_partials(uint32_t (&v)[32], const float *ws, int h0, int h1, int chunk,
+                                             int row)
+{
+    for (int hc = h0; hc < h1; ++hc) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(ws + (size_t)hc * (BN * 128)) + row;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 a = __ldcg(s4 + (chunk * 8 + i) * 128);
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + a.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + a.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + a.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16)
 {
     if (bf16) {
@@ -252,13 +329,7 @@ __device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16)
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
-// Epilogue, part 1: this thread's accumulator row of the tile (tensor-memory
-// lane `row_taddr`, columns [0, BN)) -> packed 16-bit output pairs in
-// registers, alpha applied; with SwiGLU, output column c of the tile is
-// silu(alpha * acc[c]) * alpha * acc[c + BN/2].  Column chunks at or past N
-// (input columns) are skipped.  Every lane of the warp takes part (the
-// tensor-memory loads are warp-collective).
-// Epilogue, part 2 for a CTA's last tile (the operand ring is idle): the
+// Epilogue stores of a CTA's last tile (the operand ring is idle): the
 // warp's 32 rows x `ocols` output columns as 64-column blocks of 32 rows x
 // 128 bytes with the 128-byte swizzle (16-byte chunk q of row r at q ^ (r % 8):
 // conflict-free), then a single 3-D tensor store for the warp -- one TMA
@@ -287,9 +358,17 @@ __device__ __forceinline__ void store_slab_wide(const CUtensorMap *tm, uint32_t 
     __syncwarp();
 }
 
-template <int BN, bool EPI_EX>
+// Epilogue, part 1: this thread's accumulator row of the tile (tensor-memory
+// lane `row_taddr`, columns [0, BN)) -> packed 16-bit output pairs in
+// registers, alpha applied; with SwiGLU, output column c of the tile is
+// silu(alpha * acc[c]) * alpha * acc[c + BN/2].  Column chunks at or past N
+// (input columns) are skipped.  Every lane of the warp takes part (the
+// tensor-memory loads are warp-collective).  With stream-K (SK) the partial
+// sums of CTAs [h0, h1) are added to the accumulator first.
+template <int BN, bool EPI_EX, bool SK = false>
 __device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32_t row_taddr, int n0,
-                                              int N, uint32_t (&h)[BN / 2])
+                                              int N, uint32_t (&h)[BN / 2], int h0 = 0, int h1 = 0,
+                                              int row = 0)
 {
     if constexpr (!EPI_EX) {
         // plain FP16
@@ -299,6 +378,8 @@ __device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, v);
                 ptx::tmem_wait_ld();
+                if constexpr (SK)
+                    add_partials<BN>(v, p.sk_ws, h0, h1, c, row);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     h[c * 16 + i] = pack_out2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), false);
@@ -315,6 +396,8 @@ __device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, v);
                 ptx::tmem_wait_ld();
+                if constexpr (SK)
+                    add_partials<BN>(v, p.sk_ws, h0, h1, c, row);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     h[c * 16 + i] = pack_out2(alpha * __uint_as_float(v[2 * i]),
@@ -328,6 +411,10 @@ __device__ __forceinline__ void epilogue_load(const GemmParams &p, int g, uint32
             ptx::tmem_ld_32x32b_x32(row_taddr + c * 32, gv);
             ptx::tmem_ld_32x32b_x32(row_taddr + BN / 2 + c * 32, uv);
             ptx::tmem_wait_ld();
+            if constexpr (SK) {
+                add_partials<BN>(gv, p.sk_ws, h0, h1, c, row);
+                add_partials<BN>(uv, p.sk_ws, h0, h1, c + BN / 64, row);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float o0 = silu(alpha * __uint_as_float(gv[2 * i])) * (alpha * __uint_as_float(uv[2 * i]));
@@ -355,34 +442,80 @@ __device__ __forceinline__ int kblocks_in_stage(int kchunks, int it)
     return left < BK / kMmaK ? left : BK / kMmaK;
 }
 
-// walks the (tile, k-stage) sequence of one CTA: the same order the loads
-// use, so a second cursor can run ahead of them for L2 prefetches
-template <int BK>
-struct StageCursor {
-    int t, it, g, nst;
-    TileCoord tc;
-    __device__ __forceinline__ void start(const GemmParams &p, int first_tile)
+// A piece of a CTA's work: stages [it0, it1) of the nst stages of tile
+// (g, bm, bn).  Whole tiles unless the launch is stream-K, where a tile may
+// be cut between CTAs; u1 is then the unit just past the tile's last stage.
+struct Piece {
+    int g, bm, bn;
+    int it0, it1, nst;
+    int u1;
+};
+
+// first unit of CTA c's stream-K range
+__device__ __forceinline__ int sk_begin(const GemmParams &p, int c)
+{
+    return (int)(((long long)c * p.units_total) / (long long)gridDim.x);
+}
+
+// Walks the pieces of one CTA in order: tiles blockIdx.x, + gridDim.x, ...
+// whole (SK = false), or the CTA's contiguous range of units (SK = true),
+// whose first piece may start and whose last piece may end inside a tile.
+// Every role of the CTA walks the same sequence.
+template <int BK, bool SK>
+struct PieceCursor {
+    int g, t, u, e;
+    __device__ __forceinline__ void start(const GemmParams &p)
     {
-        t = first_tile;
-        it = 0;
         g = 0;
-        nst = 0;
-        if (t < p.total_tiles) {
-            tc = tile_coord(p, t, g);
-            nst = stages_of<BK>(p.kchunks[tc.g]);
+        if constexpr (SK) {
+            u = sk_begin(p, blockIdx.x);
+            e = sk_begin(p, blockIdx.x + 1);
+        } else {
+            t = blockIdx.x;
         }
     }
-    __device__ __forceinline__ bool valid(const GemmParams &p) const { return t < p.total_tiles; }
-    __device__ __forceinline__ void advance(const GemmParams &p)
+    __device__ __forceinline__ bool next(const GemmParams &p, Piece &pc)
     {
-        if (++it == nst) {
-            it = 0;
+        if constexpr (!SK) {
+            if (t >= p.total_tiles)
+                return false;
+            const TileCoord tc = tile_coord(p, t, g);
+            pc.g = tc.g;
+            pc.bm = tc.bm;
+            pc.bn = tc.bn;
+            pc.nst = stages_of<BK>(p.kchunks[tc.g]);
+            pc.it0 = 0;
+            pc.it1 = pc.nst;
+            pc.u1 = 0;
             t += gridDim.x;
-            if (t < p.total_tiles) {
-                tc = tile_coord(p, t, g);
-                nst = stages_of<BK>(p.kchunks[tc.g]);
-            }
+            return true;
+        } else {
+            if (u >= e)
+                return false;
+            while (u >= p.unit_end[g])
+                ++g;
+            const int ub = g > 0 ? p.unit_end[g - 1] : 0;
+            const int nst = stages_of<BK>(p.kchunks[g]);
+            const int local = u - ub;
+            const int lt = local / nst;
+            pc.g = g;
+            pc.bm = lt % p.grid_m[g];
+            pc.bn = lt / p.grid_m[g];
+            pc.nst = nst;
+            pc.it0 = local - lt * nst;
+            pc.it1 = (nst - pc.it0 < e - u) ? nst : pc.it0 + (e - u);
+            pc.u1 = ub + (lt + 1) * nst;
+            u += pc.it1 - pc.it0;
+            return true;
         }
+    }
+    // after next(): the piece just returned is this CTA's last
+    __device__ __forceinline__ bool done(const GemmParams &p) const
+    {
+        if constexpr (SK)
+            return u >= e;
+        else
+            return t >= p.total_tiles;
     }
 };
 
@@ -391,7 +524,7 @@ struct StageCursor {
 // (both on sf_full[slot]).  One arrive.expect_tx and one TMA operation per
 // stage; boxes that reach past K or past the rows land as zeros and still
 // count their full size.
-template <class Cfg, int ROLE>
+template <class Cfg, bool SK, int ROLE>
 __device__ __forceinline__ void loader_role(const KernelParams &kp, uint32_t base, uint32_t bar0,
                                             const WaitCtx &wctx)
 {
@@ -418,11 +551,11 @@ __device__ __forceinline__ void loader_role(const KernelParams &kp, uint32_t bas
     uint32_t q = 0;   // position in this CTA's sequence of stages
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
-    int g = 0;
-    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t, g);
-        const int nst = stages_of<Cfg::BK>(p.kchunks[tc.g]);
-        for (int it = 0; it < nst; ++it, ++q) {
+    PieceCursor<Cfg::BK, SK> cur;
+    cur.start(p);
+    Piece tc;
+    while (ok && cur.next(p, tc)) {
+        for (int it = tc.it0; it < tc.it1; ++it, ++q) {
             const int stage = (int)(q % S);
             const uint32_t phase = (q / S) & 1u;
             if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx, kRoleProducer)) {
@@ -464,7 +597,7 @@ __device__ __forceinline__ void loader_role(const KernelParams &kp, uint32_t bas
 // the shared-memory ring holds.  It only ever delays itself: it gives up
 // (without an error) when a wait for progress exceeds the wait timeout or
 // another role aborted.
-template <class Cfg>
+template <class Cfg, bool SK>
 __device__ __forceinline__ void prefetch_role(const KernelParams &kp, volatile uint32_t *progress,
                                               const WaitCtx &wctx)
 {
@@ -472,28 +605,29 @@ __device__ __forceinline__ void prefetch_role(const KernelParams &kp, volatile u
     const uint64_t pol = p.b_policy == 1   ? ptx::policy_evict_first()
                          : p.b_policy == 2 ? ptx::policy_evict_last()
                                            : ptx::policy_evict_normal();
-    StageCursor<Cfg::BK> c;
-    c.start(p, blockIdx.x);
+    PieceCursor<Cfg::BK, SK> cur;
+    cur.start(p);
+    Piece pc;
     uint32_t q = 0;
-    while (c.valid(p)) {
-        if (q >= *progress + (uint32_t)p.pf_stages) {
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (q >= *progress + (uint32_t)p.pf_stages) {
-                if (*wctx.abort || ptx::globaltimer_ns() - t0 > wctx.timeout_ns)
-                    return;
-                __nanosleep(128);
+    while (cur.next(p, pc)) {
+        for (int it = pc.it0; it < pc.it1; ++it, ++q) {
+            if (q >= *progress + (uint32_t)p.pf_stages) {
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (q >= *progress + (uint32_t)p.pf_stages) {
+                    if (*wctx.abort || ptx::globaltimer_ns() - t0 > wctx.timeout_ns)
+                        return;
+                    __nanosleep(128);
+                }
             }
+            ptx::tma_prefetch_3d(&p.tmB[pc.g], 0, pc.bn * Cfg::BN, it * Cfg::kChunks, pol);
+            ptx::tma_prefetch_3d(&kp.tmSFB[pc.g], 0, it * Cfg::kMmas, pc.bn * (Cfg::BN / 128), pol);
         }
-        ptx::tma_prefetch_3d(&p.tmB[c.tc.g], 0, c.tc.bn * Cfg::BN, c.it * Cfg::kChunks, pol);
-        ptx::tma_prefetch_3d(&kp.tmSFB[c.tc.g], 0, c.it * Cfg::kMmas, c.tc.bn * (Cfg::BN / 128), pol);
-        c.advance(p);
-        ++q;
     }
 }
 
 // EPI_EX: the fused epilogue options (alpha, BF16, SwiGLU) are compiled in;
 // the plain FP16 form keeps the default path's register budget.
-template <class Cfg, bool EPI_EX>
+template <class Cfg, bool EPI_EX, bool SK>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     nvfp4_group_gemm_kernel(const __grid_constant__ KernelParams kp)
 {
@@ -554,18 +688,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::grid_launch_dependents();
 
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};
-    const int total = p.total_tiles;
-
     if (warp == Cfg::kPrefetchWarp) {
         if (lane == 0 && p.pf_stages > 0)
-            prefetch_role<Cfg>(kp, mma_progress, wctx);
+            prefetch_role<Cfg, SK>(kp, mma_progress, wctx);
     } else if (warp >= kFirstLoaderWarp) {
         if (lane == 0) {
             switch (warp - kFirstLoaderWarp) {
-            case 0: loader_role<Cfg, 0>(kp, base, bar0, wctx); break;
-            case 1: loader_role<Cfg, 1>(kp, base, bar0, wctx); break;
-            case 2: loader_role<Cfg, 2>(kp, base, bar0, wctx); break;
-            default: loader_role<Cfg, 3>(kp, base, bar0, wctx); break;
+            case 0: loader_role<Cfg, SK, 0>(kp, base, bar0, wctx); break;
+            case 1: loader_role<Cfg, SK, 1>(kp, base, bar0, wctx); break;
+            case 2: loader_role<Cfg, SK, 2>(kp, base, bar0, wctx); break;
+            default: loader_role<Cfg, SK, 3>(kp, base, bar0, wctx); break;
             }
         }
     } else if (warp == kSfWarp) {
@@ -575,12 +707,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // slot's own tensor-memory columns and signal sf_ready[slot]
             uint32_t q = 0;
             bool ok = true, issued_any = false;
-            int g = 0;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileCoord tc = tile_coord(p, t, g);
+            PieceCursor<Cfg::BK, SK> cur;
+            cur.start(p);
+            Piece tc;
+            while (ok && cur.next(p, tc)) {
                 const int kchunks = p.kchunks[tc.g];
-                const int nst = stages_of<Cfg::BK>(kchunks);
-                for (int it = 0; it < nst; ++it, ++q) {
+                for (int it = tc.it0; it < tc.it1; ++it, ++q) {
                     const int stage = (int)(q % S);
                     if (!wait_bounded(sffull_bar(stage), (q / S) & 1u, wctx, kRoleSf)) {
                         ok = false;
@@ -618,18 +750,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            int g = 0;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileCoord tc = tile_coord(p, t, g);
+            PieceCursor<Cfg::BK, SK> cur;
+            cur.start(p);
+            Piece tc;
+            while (ok && cur.next(p, tc)) {
                 const int kchunks = p.kchunks[tc.g];
-                const int nst = stages_of<Cfg::BK>(kchunks);
                 if (!wait_bounded(acce_bar(acc), acc_phase ^ 1u, wctx, kRoleMma)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int it = 0; it < nst; ++it, ++q) {
+                for (int it = tc.it0; it < tc.it1; ++it, ++q) {
                     const int stage = (int)(q % S);
                     if (!wait_bounded(full_bar(stage), (q / S) & 1u, wctx, kRoleMma) ||
                         !wait_bounded(sfr_bar(stage), (q / S) & 1u, wctx, kRoleMma)) {
@@ -650,7 +782,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                               desc_operand_sw128(sb + koff_b), Cfg::kIdesc,
                                               tmem_base + Cfg::sfa_col(stage, j),
                                               tmem_base + Cfg::sfb_col(stage, j, 0),
-                                              (it > 0 || j > 0) ? 1u : 0u);
+                                              (it > tc.it0 || j > 0) ? 1u : 0u);
                         }
                     }
                     // frees the slot once these MMAs (and, through sf_ready,
@@ -679,11 +811,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         int sbuf = 0;
-        int g = 0;
         const uint32_t stage_buf = base + Cfg::kEpiOff + warp * Cfg::kEpiBufs * Cfg::kEpiBufBytes;
         const uint32_t lane_tmem = (uint32_t)(warp * 32) << 16;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileCoord tc = tile_coord(p, t, g);
+        const int row = warp * 32 + lane;   // accumulator row (tensor-memory lane) of this thread
+        uint32_t epoch = 0;                 // stream-K: the launch's flag value
+        if constexpr (SK)
+            epoch = *reinterpret_cast<volatile const uint32_t *>(p.sk_epoch);
+        PieceCursor<Cfg::BK, SK> cur;
+        cur.start(p);
+        Piece tc;
+        while (cur.next(p, tc)) {
             // lane 0 waits; the outcome is broadcast so the warp stays
             // converged for the .sync.aligned tensor-memory loads
             uint32_t ready = 1u;
@@ -697,11 +834,58 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int N = p.N[tc.g];
             const int m0 = tc.bm * kBM + warp * 32;
             const int n0 = tc.bn * BN;
+            const uint32_t acc_taddr = tmem_base + lane_tmem + acc * BN;
+            if constexpr (SK) {
+                if (tc.it0 > 0) {
+                    // a later part of a tile that another CTA owns: the
+                    // partial sum goes to this CTA's slot, the accumulator
+                    // back to the MMA thread, then the flag is published
+                    if (m0 < M)
+                        store_partial<BN>(p.sk_ws, acc_taddr, n0, N, row);
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(acce_bar(acc));
+                    if (m0 < M) {
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::st_release_gpu(p.sk_flags + blockIdx.x * 4 + warp, epoch);
+                    }
+                    if (++acc == Cfg::kAccBufs) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                    continue;
+                }
+            }
+            // stream-K owner of a cut tile (it holds the tile's first stages):
+            // the CTAs after this one whose ranges start inside the tile hold
+            // the rest of its sum; their ranges began with it, so their flags
+            // are normally set long before
+            int h0 = 0, h1 = 0;
+            if constexpr (SK) {
+                if (tc.it1 < tc.nst && m0 < M) {
+                    h0 = (int)blockIdx.x + 1;
+                    h1 = h0;
+                    while (h1 < (int)gridDim.x && sk_begin(p, h1) < tc.u1)
+                        ++h1;
+                    uint32_t ok = 1u;
+                    if (lane == 0)
+                        for (int hc = h0; hc < h1 && ok; ++hc)
+                            ok = wait_flag_bounded(p.sk_flags + hc * 4 + warp, epoch, wctx) ? 1u : 0u;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok)
+                        break;
+                    __syncwarp();
+                    __threadfence();
+                }
+            }
             // 1. this thread's whole accumulator row -> 16-bit output pairs in
             // registers
             uint32_t h[BN / 2];
             if (m0 < M)
-                epilogue_load<BN, EPI_EX>(p, tc.g, tmem_base + lane_tmem + acc * BN, n0, N, h);
+                epilogue_load<BN, EPI_EX, SK>(p, tc.g, acc_taddr, n0, N, h, h0, h1, row);
             // 2. every lane's loads have completed (wait::ld): the accumulator
             // goes back to the MMA thread before the stores start, so the next
             // tile's MMAs overlap them
@@ -717,7 +901,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // the CTA's last tile: every MMA has completed and no load is
             // left, so the operand ring is free -- each chunk gets its own
             // staging buffer there and the stores go out back to back
-            const bool last_tile = t + (int)gridDim.x >= total;
+            const bool last_tile = cur.done(p);
             const uint32_t ring_buf = base + (uint32_t)(warp * (BN / EC)) * Cfg::kEpiBufBytes;
             if (m0 < M && last_tile && p.c_wide[tc.g]) {
                 store_slab_wide<BN>(&p.tmCw[tc.g], base + (uint32_t)(warp * (BN / 64)) * 4096u, lane, on0, oN,
@@ -777,6 +961,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+    if constexpr (SK) {
+        // the last CTA to finish moves the epoch on (and re-arms the count),
+        // so the next launch -- which reads both only after this grid has
+        // completed -- never mistakes this launch's flags for its own
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.sk_epoch + 1, 1u) == gridDim.x - 1) {
+                volatile uint32_t *ep = p.sk_epoch;
+                ep[1] = 0u;
+                ep[0] = ep[0] + 1u;
+            }
+        }
     }
 }
 

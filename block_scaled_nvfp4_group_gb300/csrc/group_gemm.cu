@@ -29,12 +29,14 @@ enum Kind : int {
     kKindWideP2 = NVFP4_KIND_WIDE_P2,
     kKindWideP4 = NVFP4_KIND_WIDE_P4,
     kKindPair = NVFP4_KIND_PAIR,
-    kNumKinds = 7
+    kKindWideSK = NVFP4_KIND_WIDE_SK,
+    kNumKinds = 8
 };
 
 bool needs_n256(int kind)
 {
-    return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4;
+    return kind == kKindWide || kind == kKindWide512 || kind == kKindWideP2 || kind == kKindWideP4 ||
+           kind == kKindWideSK;
 }
 
 // the producer-pair variants are folded into WIDE: every stage's loads are
@@ -71,13 +73,13 @@ void make_launch_cfg(LaunchCfg &L, int grid, int threads, int smem, bool pair, c
     L.cfg.numAttrs = pair ? 2 : 1;
 }
 
-template <class Cfg>
+template <class Cfg, bool SK>
 cudaError_t launch_kind(const KernelParams &P, int grid, cudaStream_t s, bool ex)
 {
     LaunchCfg L;
     make_launch_cfg(L, grid, Cfg::kThreads, Cfg::kSmemBytes, false, s);
-    return ex ? cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, true>, P)
-              : cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, false>, P);
+    return ex ? cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, true, SK>, P)
+              : cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_kernel<Cfg, false, SK>, P);
 }
 
 template <class Cfg>
@@ -100,25 +102,27 @@ struct KindInfo {
     int threads;
     int smem;
     bool pair;
+    bool sk;             // stream-K ranges of (tile, stage) units
     const void *fn;      // plain FP16 epilogue
     const void *fn_ex;   // fused epilogue options compiled in
     cudaError_t (*launch)(const KernelParams &, int, cudaStream_t, bool);
 };
 
-template <class Cfg>
+template <class Cfg, bool SK = false>
 KindInfo make_kind()
 {
     return KindInfo{kBM, Cfg::BN, Cfg::BN, Cfg::kChunks, Cfg::kMmas, Cfg::BN / 128, Cfg::kEpiCols,
-                    Cfg::kThreads, Cfg::kSmemBytes, false,
-                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, false>),
-                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, true>), &launch_kind<Cfg>};
+                    Cfg::kThreads, Cfg::kSmemBytes, false, SK,
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, false, SK>),
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_kernel<Cfg, true, SK>),
+                    &launch_kind<Cfg, SK>};
 }
 
 template <class Cfg>
 KindInfo make_pair_kind()
 {
     return KindInfo{Cfg::kPairBM, Cfg::BN, Cfg::BN / 2, 1, Cfg::kMmas, Cfg::kSfRb, Cfg::kEpiCols,
-                    Cfg::kThreads, Cfg::kSmemBytes, true,
+                    Cfg::kThreads, Cfg::kSmemBytes, true, false,
                     reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg, false>),
                     reinterpret_cast<const void *>(&nvfp4_group_gemm_pair_kernel<Cfg, true>),
                     &launch_pair_kind<Cfg>};
@@ -129,7 +133,7 @@ const KindInfo &kind_info(int k)
     static const KindInfo table[kNumKinds] = {
         make_kind<CfgStream>(),  make_kind<CfgWide>(), make_kind<CfgCompute>(),
         make_kind<CfgWide512>(), make_kind<CfgWide>(), make_kind<CfgWide>(),
-        make_pair_kind<CfgPair>()};
+        make_pair_kind<CfgPair>(), make_kind<CfgWide, true>()};
     return table[canonical_kind(k)];
 }
 
@@ -213,8 +217,13 @@ int validate_call(const GroupDesc *groups, int num_groups)
 // 256 x 256 tile in about 0.92 of the time one CTA takes for a 128 x 256
 // tile, but pad M to 256: they are chosen when the call fills at least four
 // rounds of the grid and pairing does not add a round (large M, e.g. the
-// 4096^3 groups), never for the small-M MoE shapes.  NVFP4_GEMM_KIND
-// overrides the choice.
+// 4096^3 groups), never for the small-M MoE shapes.  Stream-K (WIDE_SK) is
+// never chosen here: on GB300 it measured slower than whole tiles even where
+// it removes the most idle time (fewer tiles than SMs: 2 groups of 512 x
+// 3072 x 4096, 37.8 vs 21.0 us): its ranges start at scattered K offsets, so
+// the first loads pull far more distinct bytes from HBM, each stage then
+// competes with 152 instead of 96 CTAs, and the cut tiles add a partial-sum
+// exchange.  NVFP4_GEMM_KIND overrides the choice.
 int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = false)
 {
     const int forced_env = env_int("NVFP4_GEMM_KIND", -1);
@@ -239,6 +248,16 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
         // a pair's B scale load spans two 128-row blocks: N >= 256
         if (forced == kKindPair && !all_n_ge256)
             return kKindStream;
+        // stream-K unit indices are 32-bit
+        if (forced == kKindWideSK) {
+            long long units = 0;
+            for (int i = 0; i < n; ++i)
+                if (groups[i].M > 0)
+                    units += (long long)((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256) *
+                             (groups[i].K / 256);
+            if (units >= (1ll << 30))
+                return kKindWide;
+        }
         return forced;
     }
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
@@ -295,7 +314,8 @@ int count_launches(const GroupDesc *groups, int num_groups, int bm, int bn)
 // live in a per-thread vector whose capacity is kept between calls.
 template <class ErrFn>
 int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
-                    int sm_count, int kind, ErrFn err_for_launch, const GemmEpilogue *epi = nullptr)
+                    int sm_count, int kind, ErrFn err_for_launch, const GemmEpilogue *epi = nullptr,
+                    const SkScratch *sk = nullptr)
 {
     const bool swiglu = epi && epi->swiglu;
     const bool out_bf16 = epi && epi->out_bf16;
@@ -333,6 +353,11 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
             P.debug_drop_stage = drop;
             P.out_bf16 = out_bf16 ? 1 : 0;
             P.swiglu = swiglu ? 1 : 0;
+            if (ki.sk) {
+                P.sk_ws = sk->ws;
+                P.sk_flags = sk->flags;
+                P.sk_epoch = sk->epoch;
+            }
         }
         KernelParams &PP = plist.back();
         GemmParams &P = PP.g;
@@ -367,11 +392,18 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
         P.grid_m[j] = grid_m;
         P.total_tiles += (int)tiles;
         P.tile_end[j] = P.total_tiles;
+        if (ki.sk) {
+            const int bk = ki.chunks * kChunkK;
+            P.units_total += (int)tiles * ((g.K + bk - 1) / bk);
+            P.unit_end[j] = P.units_total;
+        }
         P.num_groups = j + 1;
     }
     for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
         const KernelParams &P = plist[l];
-        const int grid = grid_size(dev, kind, P.g.total_tiles, sm_count);
+        // stream-K: one range of units per SM (at least one unit each)
+        const int grid = ki.sk ? (P.g.units_total < sm_count ? P.g.units_total : sm_count)
+                               : grid_size(dev, kind, P.g.total_tiles, sm_count);
         if (ki.launch(P, grid, stream, ex) != cudaSuccess || cudaGetLastError() != cudaSuccess)
             rc = NVFP4_ERR_CUDA;
     }
@@ -391,9 +423,12 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
     rc = current_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
-    const int kind = choose_kind(groups, num_groups, dev->sm_count);
+    int kind = choose_kind(groups, num_groups, dev->sm_count);
     if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
         return NVFP4_OK;
+    SkScratch sk{};
+    if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
+        kind = kKindWide;
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     rc = ensure_kernel_attributes(dev_id, kind);
@@ -401,7 +436,7 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
         return rc;
     uint32_t *err = dev->err;
     return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
-                           [err](int) { return err; });
+                           [err](int) { return err; }, nullptr, &sk);
 }
 
 extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilogue *epi,
@@ -420,9 +455,12 @@ extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, cons
     rc = current_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
-    const int kind = choose_kind(groups, num_groups, dev->sm_count, swiglu);
+    int kind = choose_kind(groups, num_groups, dev->sm_count, swiglu);
     if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
         return NVFP4_OK;
+    SkScratch sk{};
+    if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
+        kind = kKindWide;
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     rc = ensure_kernel_attributes(dev_id, kind);
@@ -430,7 +468,7 @@ extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, cons
         return rc;
     uint32_t *err = dev->err;
     return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
-                           [err](int) { return err; }, epi);
+                           [err](int) { return err; }, epi, &sk);
 }
 
 extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind,
@@ -525,7 +563,10 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
     rc = noalloc_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
-    const int kind = choose_kind(groups, num_groups, dev->sm_count);
+    // no stream-K here: its partial sums need allocated scratch
+    int kind = choose_kind(groups, num_groups, dev->sm_count);
+    if (kind == kKindWideSK)
+        kind = kKindWide;
     // each launch needs its own two status words of the static scratch
     const int launches = count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn);
     if (launches == 0)

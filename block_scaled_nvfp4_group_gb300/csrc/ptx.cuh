@@ -144,6 +144,19 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int
                  : "memory");
 }
 
+// release store / acquire load of a 32-bit flag in global memory, GPU scope
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // 3-D tiled store shared -> global (elements outside the tensor are not
 // written)
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int x, int y, int z)

@@ -7,8 +7,10 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "../../include/nvfp4_group_gemm.h"
 
@@ -177,6 +179,48 @@ int encode_map_c_wide(CUtensorMap *out, CUtensorMapDataType dtype, const void *p
     const MapKey key{ptr, 64, rows, cols / 64, cols * 2, 128, 64, 32, box_blocks, 3, (int)dtype,
                      (int)CU_TENSOR_MAP_SWIZZLE_128B};
     return encode_map(out, key);
+}
+
+namespace {
+std::mutex g_sk_mu;
+std::map<std::pair<int, cudaStream_t>, SkScratch> g_sk;
+}  // namespace
+
+int sk_scratch(cudaStream_t stream, int slots, SkScratch *out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_sk_mu);
+    auto it = g_sk.find({dev, stream});
+    if (it != g_sk.end() && it->second.slots >= slots) {
+        *out = it->second;
+        return NVFP4_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return NVFP4_ERR_UNSUPPORTED;
+    const size_t ws_bytes = (size_t)slots * 128 * 256 * sizeof(float);
+    const size_t flag_bytes = (size_t)slots * 4 * sizeof(uint32_t);
+    void *mem = nullptr;
+    if (cudaMalloc(&mem, ws_bytes + flag_bytes + 16) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    SkScratch s;
+    s.ws = static_cast<float *>(mem);
+    s.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(mem) + ws_bytes);
+    s.epoch = reinterpret_cast<uint32_t *>(static_cast<char *>(mem) + ws_bytes + flag_bytes);
+    s.slots = slots;
+    // flags all ones, epoch 0: no flag matches before a partial is written
+    if (cudaMemsetAsync(s.flags, 0xFF, flag_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(s.epoch, 0, 16, stream) != cudaSuccess) {
+        cudaFree(mem);
+        return NVFP4_ERR_CUDA;
+    }
+    // a smaller area of this stream is left in place: launches already
+    // queued on the stream may still use it
+    g_sk[{dev, stream}] = s;
+    *out = s;
+    return NVFP4_OK;
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }

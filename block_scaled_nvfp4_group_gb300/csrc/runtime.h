@@ -47,6 +47,19 @@ int encode_map_sf(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t K, 
 int encode_map_c_wide(CUtensorMap *out, CUtensorMapDataType dtype, const void *ptr, uint64_t rows,
                       uint64_t cols, uint32_t box_blocks);
 
+// Stream-K scratch of one (device, stream): `slots` partial-sum slots of
+// 128 x 256 FP32, four flag words per slot (set to all ones at allocation)
+// and the launch epoch with its finished-CTA count (both zero).  Allocated on
+// the first request for the pair, never while the stream is capturing a
+// graph; kept until the process exits.  Returns an NVFP4_* code.
+struct SkScratch {
+    float *ws;
+    uint32_t *flags;
+    uint32_t *epoch;
+    int slots;
+};
+int sk_scratch(cudaStream_t stream, int slots, SkScratch *out);
+
 unsigned long long wait_timeout_ns();
 int debug_drop_stage();
 int b_policy_override();   // -1 = use the built-in choice

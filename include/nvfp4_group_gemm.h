@@ -113,7 +113,20 @@ int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilo
  *          configuration spreads a stage's loads over four issuing warps)
  *  PAIR    256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; N >= 256):
  *          chosen for large M, when pairing fills at least four rounds of
- *          the grid without adding one */
+ *          the grid without adding one
+ *  WIDE_SK WIDE tiles with stream-K: the call's (tile, 256-K stage) units
+ *          are cut into one equal contiguous range per SM, so a tile may be
+ *          split between CTAs; the CTA holding a tile's first stages adds
+ *          the FP32 partial sums of the others before its epilogue.  Only
+ *          selected through NVFP4_GEMM_KIND=7: on GB300 whole tiles measured
+ *          faster even with fewer tiles than SMs.  Needs a scratch area per
+ *          stream (one 128 KiB partial-sum slot per SM and a few flag
+ *          words), allocated on the first such call on that stream and kept
+ *          until the process exits; when it cannot be allocated (e.g. the
+ *          stream is being captured into a graph at that moment) the call
+ *          runs as WIDE.  Sums of cut tiles are formed in a different order,
+ *          so results may differ from WIDE in the last bits of FP32 before
+ *          rounding. */
 enum {
     NVFP4_KIND_STREAM = 0,
     NVFP4_KIND_WIDE = 1,
@@ -121,7 +134,8 @@ enum {
     NVFP4_KIND_WIDE512 = 3,
     NVFP4_KIND_WIDE_P2 = 4,
     NVFP4_KIND_WIDE_P4 = 5,
-    NVFP4_KIND_PAIR = 6
+    NVFP4_KIND_PAIR = 6,
+    NVFP4_KIND_WIDE_SK = 7
 };
 
 /* The plan nvfp4_group_gemm would follow for these groups on the current
