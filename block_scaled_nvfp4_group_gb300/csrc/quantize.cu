@@ -14,13 +14,26 @@
 // scale rounds to 0 gets codes 0.  The conversions are the hardware's
 // cvt.rn.satfinite to e4m3x2 / e2m1x2.
 //
-// One CTA of 128 threads takes one 128-row block and one 64-element K block
-// (one 512-byte scale atom): thread t reads row t's 128 bytes of input, writes
-// its 32 bytes of codes, and its four scales into the atom staged in shared
-// memory; one warp then stores the atom with 16-byte stores.  Algorithmic
-// traffic: 2 bytes read and 0.5 + 1/16 (+ 1/16 row-major) bytes written per
-// element; the exact single-precision division per element makes it about
-// 20 instructions per element, so issue and memory latency share the bound.
+// One CTA of 128 threads takes a 128-row block and 128 columns (two scale
+// atoms; narrower tiles than a whole row leave a smaller last round of CTAs).
+// Warp w walks rows 32 w .. 32 w + 31, two rows per step: lane i loads
+// columns 8 (i % 16) .. + 7 of row 2 s + i / 16 (one 16-byte load; a warp
+// reads two 256-byte row pieces), eight steps in flight.  Lanes 2 j and
+// 2 j + 1 share 16-element block j (absmax through one shuffle), and the
+// lane's eight codes go out as one 4-byte store.  Scales are staged in shared memory in the
+// tiled atom layout (and row-major) and leave in 16-byte stores at the end.
+// The quotients absmax / 6 and x / scale are formed as q = a r with r = 1 /
+// divisor correctly rounded (a constant, or a 128-entry shared-memory table
+// of __frcp_rn over the E4M3 codes, filled at block start beside the decoded
+// scales), refined by one Newton correction q + (a - q divisor) r with fused
+// multiply-adds (the classic division refinement of Markstein, IBM J. Res.
+// Dev. 34(1), 1990).  It equals the correctly rounded IEEE quotient wherever
+// that decides the E4M3 / E2M1 code: an exact quotient (every tie is one) is
+// recovered exactly, and any other quotient of these operands lies far
+// (relatively ~2^-15) from a rounding threshold compared with the
+// refinement's error.  Checked against the IEEE division for every finite
+// FP16 and BF16 value (and every E4M3 scale), and byte for byte against the
+// oracle in the tests.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -36,7 +49,12 @@ namespace {
 
 constexpr int kMaxDim = 1 << 20;
 constexpr int kRows = 128;       // rows per CTA (one scale row block)
-constexpr int kColsPerCta = 64;  // K elements per CTA (one scale atom)
+constexpr int kCols = 128;       // K elements per CTA (two scale atoms)
+constexpr int kThreads = 128;
+constexpr int kLanesPerRow = kCols / 8;
+constexpr int kRowsPerStep = 32 / kLanesPerRow;
+constexpr int kUnroll = 8;       // steps in flight per warp
+static_assert(kThreads == 128, "one thread per E4M3 code fills the scale tables");
 
 __device__ __forceinline__ uint32_t e4m3_of(float s)
 {
@@ -54,19 +72,22 @@ __device__ __forceinline__ float e4m3_value(uint32_t e)
     return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
-// E2M1 codes of (lo, hi), lo in bits 0..3; a zero magnitude loses its sign
+// E2M1 codes of (lo, hi) in bits 0..3 and 4..7
 __device__ __forceinline__ uint32_t e2m1x2_of(float lo, float hi)
 {
     uint32_t r;
     asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tmov.b32 %0, {t, 0, 0, 0};\n\t}"
         : "=r"(r)
         : "f"(hi), "f"(lo));
-    r &= 0xFFu;
-    if ((r & 0x7u) == 0)
-        r &= 0xF0u;
-    if ((r & 0x70u) == 0)
-        r &= 0x0Fu;
-    return r;
+    return r & 0xFFu;
+}
+
+// eight codes in a word: a zero magnitude loses its sign bit
+__device__ __forceinline__ uint32_t clear_negative_zeros(uint32_t w)
+{
+    const uint32_t mag = w & 0x77777777u;
+    const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;   // bit 3 of each nibble: magnitude != 0
+    return mag | (w & nonzero);
 }
 
 template <bool BF16>
@@ -79,8 +100,9 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
             f[2 * i] = __uint_as_float(w[i] << 16);
             f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
         } else {
-            f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFFu)));
-            f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
         }
     }
 }
@@ -93,64 +115,95 @@ struct QuantParams {
     int rows, K;
 };
 
-// One CTA: 128 rows x 64 elements (one scale atom); thread t takes row t:
-// eight 16-byte loads (its whole 128-byte row segment, issued before the
-// first use), four 16-element blocks, 32 bytes of codes in two 16-byte
-// stores, and its four scales into the atom staged in shared memory.
 template <bool BF16>
-__global__ void __launch_bounds__(kRows) quantize_kernel(const __grid_constant__ QuantParams p)
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constant__ QuantParams p)
 {
-    __shared__ __align__(16) uint32_t atom[kRows];   // 512 bytes
+    __shared__ __align__(16) uint8_t atoms[kCols / 64][512];   // the tile's scale atoms
+    __shared__ __align__(16) uint8_t rm[kRows][kCols / 16];    // the same scales, row-major
+    __shared__ float dec[128], rcp[128];                        // E4M3 code -> value, 1 / value
+    {
+        const uint32_t c = threadIdx.x;   // kThreads == 128: one code each (127 is NaN, never produced)
+        const float v = c < 127 ? e4m3_value(c) : 0.0f;
+        dec[c] = v;
+        rcp[c] = v > 0.0f ? __frcp_rn(v) : 0.0f;
+    }
+    __syncthreads();
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    const int kb = blockIdx.x;                  // 64-element K block
+    const int c0 = blockIdx.x * kCols;          // first column of the tile
     const int rb = blockIdx.y;                  // 128-row block
-    const int t = threadIdx.x;
-    const int r = rb * kRows + t;
-    uint32_t sfw = 0;                           // the row's four scales
-    if (r < p.rows) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)r * p.K + (size_t)kb * kColsPerCta);
-        uint4 v[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int piece = lane % kLanesPerRow;     // 8-column piece of the tile
+    const int sub = lane / kLanesPerRow;        // row of the step
+    const int col = c0 + 8 * piece;             // this lane's first column
+    const bool in_k = col < p.K;                // K % 64 == 0: whole 8-column pieces
+    const int j = piece >> 1;                   // 16-element block of the tile
+    for (int rr = 0; rr < 32; rr += kUnroll * kRowsPerStep) {
+        uint4 v[kUnroll];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = __ldg(src + i);
-        uint32_t cw[8];                         // 32 bytes of codes
+        for (int u = 0; u < kUnroll; ++u) {
+            const int row = rb * kRows + warp * 32 + rr + u * kRowsPerStep + sub;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (in_k && row < p.rows)
+                v[u] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)row * p.K + col));
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {           // 16-element blocks
-            float lo8[8], hi8[8];
-            unpack8<BF16>(v[2 * j], lo8);
-            unpack8<BF16>(v[2 * j + 1], hi8);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int lr = warp * 32 + rr + u * kRowsPerStep + sub;   // row within the block
+            const int row = rb * kRows + lr;
+            float f[8];
+            unpack8<BF16>(v[u], f);
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                amax = fmaxf(amax, fmaxf(fabsf(lo8[i]), fabsf(hi8[i])));
-            const uint32_t sc = e4m3_of(amax / 6.0f);
-            const float sdec = e4m3_value(sc);
-            sfw |= sc << (8 * j);
-            uint32_t b[8];
+                amax = fmaxf(amax, fabsf(f[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            constexpr float kSixth = 1.0f / 6.0f;
+            const float a0 = amax * kSixth;
+            const uint32_t sc = e4m3_of(fmaf(fmaf(-a0, 6.0f, amax), kSixth, a0));
+            const float sdec = dec[sc];
+            uint32_t w = 0;
+            if (sdec > 0.0f) {
+                const float r = rcp[sc];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                b[i] = sdec > 0.0f ? e2m1x2_of(lo8[2 * i] / sdec, lo8[2 * i + 1] / sdec) : 0u;
-                b[4 + i] = sdec > 0.0f ? e2m1x2_of(hi8[2 * i] / sdec, hi8[2 * i + 1] / sdec) : 0u;
+                for (int i = 0; i < 4; ++i) {
+                    float q[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float x = f[2 * i + h];
+                        const float q0 = x * r;
+                        q[h] = fmaf(fmaf(-q0, sdec, x), r, q0);
+                    }
+                    w |= e2m1x2_of(q[0], q[1]) << (8 * i);
+                }
+                w = clear_negative_zeros(w);
             }
-            cw[2 * j] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-            cw[2 * j + 1] = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+            if (in_k && row < p.rows)
+                *reinterpret_cast<uint32_t *>(p.codes + (size_t)row * (p.K / 2) + col / 2) = w;
+            if ((lane & 1) == 0) {
+                // rows past `rows` leave zero scales (amax 0)
+                atoms[j >> 2][(lr % 32) * 16 + (lr / 32) * 4 + (j & 3)] = (uint8_t)sc;
+                rm[lr][j] = (uint8_t)sc;
+            }
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(p.codes + (size_t)r * (p.K / 2) + (size_t)kb * (kColsPerCta / 2));
-        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        if (p.sf_rowmajor)
-            *reinterpret_cast<uint32_t *>(p.sf_rowmajor + (size_t)r * (p.K / 16) + (size_t)kb * 4) = sfw;
     }
-    // row t's four scales at byte (t % 32) * 16 + (t / 32) * 4 of the atom;
-    // rows past `rows` stay zero
-    atom[(t % 32) * 4 + t / 32] = sfw;
     __syncthreads();
-    if (t < 32) {
-        const uint4 w = reinterpret_cast<const uint4 *>(atom)[t];
-        uint4 *dst = reinterpret_cast<uint4 *>(p.sf_tiled + ((size_t)rb * (p.K / 64) + kb) * 512);
-        dst[t] = w;
+    // the tile's atoms are contiguous in the tiled layout: 16 bytes per thread
+    const int natoms = min(kCols / 64, (p.K - c0) / 64);
+    const int t = threadIdx.x;
+    if (t * 16 < natoms * 512) {
+        uint8_t *dst = p.sf_tiled + ((size_t)rb * (p.K / 64) + c0 / 64) * 512;
+        *reinterpret_cast<uint4 *>(dst + t * 16) = *reinterpret_cast<const uint4 *>(&atoms[0][0] + t * 16);
+    }
+    if (p.sf_rowmajor) {
+        const int row = rb * kRows + t;
+        if (row < p.rows) {
+            uint8_t *dst = p.sf_rowmajor + (size_t)row * (p.K / 16) + c0 / 16;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(rm[t]);
+            for (int a = 0; a < natoms; ++a)
+                *reinterpret_cast<uint32_t *>(dst + 4 * a) = src[a];
+        }
     }
 }
 
@@ -161,7 +214,7 @@ extern "C" int nvfp4_quantize(const void *x, int x_is_bf16, int rows, int K, voi
                               void *sf_rowmajor, cudaStream_t stream)
 {
     using namespace nvfp4;
-    if (rows < 0 || K <= 0 || K % kColsPerCta != 0 || rows > kMaxDim || K > kMaxDim)
+    if (rows < 0 || K <= 0 || K % 64 != 0 || rows > kMaxDim || K > kMaxDim)
         return NVFP4_ERR_INVALID_ARGUMENT;
     if (rows == 0)
         return NVFP4_OK;
@@ -181,8 +234,8 @@ extern "C" int nvfp4_quantize(const void *x, int x_is_bf16, int rows, int K, voi
     p.rows = rows;
     p.K = K;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(K / kColsPerCta, (rows + kRows - 1) / kRows);
-    cfg.blockDim = dim3(kRows);
+    cfg.gridDim = dim3((K + kCols - 1) / kCols, (rows + kRows - 1) / kRows);
+    cfg.blockDim = dim3(kThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -121,3 +121,37 @@ def test_rejects_bad_shapes():
         _abi.NVFP4_ERR_MISALIGNED
     assert lib.nvfp4_quantize(x.data_ptr(), 0, 0, 64, c.data_ptr(), s.data_ptr(), None, None) == \
         _abi.NVFP4_OK
+
+
+def _exhaustive_blocks(bf16: bool) -> np.ndarray:
+    """16-element blocks that hit every positive E4M3FN scale s: each block is
+    [6 s, x_1 .. x_15] with the x_i running through every finite FP16 (or
+    BF16) magnitude in [0, 6 s], alternately negated, so every code and tie
+    of every scale is formed (absmax 6 s gives exactly the scale s)."""
+    o = oracle.get()
+    dec = [o.e4m3fn(c) for c in range(128)]
+    if bf16:
+        mags = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        mags = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    blocks = []
+    for code in range(1, 127):
+        s = dec[code]
+        a = 6.0 * s
+        xs = mags[mags <= a]
+        xs = np.where(np.arange(xs.size) % 2 == 1, -xs, xs)
+        pad = (-xs.size) % 15
+        xs = np.concatenate([xs, np.zeros(pad)]).reshape(-1, 15)
+        blocks.append(np.concatenate([np.full((xs.shape[0], 1), a), xs], axis=1))
+    return np.concatenate(blocks).reshape(-1)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_exhaustive_values_and_scales(bf16):
+    """Every finite FP16 / BF16 magnitude against every E4M3 scale it can
+    meet, through the kernel, byte for byte against the oracle."""
+    vals = _exhaustive_blocks(bf16)
+    K = 4096
+    vals = np.concatenate([vals, np.zeros((-vals.size) % K)])
+    x = vals.reshape(-1, K)
+    _check(x, bf16, f"exhaustive {'bf16' if bf16 else 'fp16'} {x.shape}")
