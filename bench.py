@@ -39,14 +39,16 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio, GB300
 # capture, keyed by workload, valid only for the kernel source it was taken
 # on (sha256 prefix over the GEMM's source files).  From profiles/.
 NCU_TRAFFIC = {
-    "moe_gate_up": {"bytes": 140451328 + 7343360, "kernel_sha": "d16288c56cc3778e",
+    "moe_gate_up": {"bytes": 140452352 + 7452672, "kernel_sha": "8535f728de53a59f",
                     "source": "profiles/gemm_moe_gate_up.md"},
-    "square": {"bytes": 75577344 + 94339072, "kernel_sha": "d16288c56cc3778e",
+    "moe_down": {"bytes": 68543744 + 4455680, "kernel_sha": "8535f728de53a59f",
+                 "source": "profiles/gemm_moe_down.md"},
+    "quantized": {"bytes": 16568576 + 0, "kernel_sha": "8535f728de53a59f",
+                  "source": "profiles/gemm_quantized.md"},
+    "square": {"bytes": 75608576 + 92040704, "kernel_sha": "8535f728de53a59f",
                "source": "profiles/gemm_square.md"},
-    "moe_down": {"bytes": 68545280 + 4397824, "kernel_sha": "d16288c56cc3778e",
-                 "source": "profiles/traffic_gemm.md"},
-    "quantized": {"bytes": 16569856 + 0, "kernel_sha": "d16288c56cc3778e",
-                  "source": "profiles/traffic_gemm.md"},
+    "tiny": {"bytes": 155904 + 0, "kernel_sha": "8535f728de53a59f",
+             "source": "profiles/gemm_tiny.md"},
 }
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "group_gemm.cu", "ptx.cuh")
 
