@@ -155,3 +155,23 @@ def test_exhaustive_values_and_scales(bf16):
     vals = np.concatenate([vals, np.zeros((-vals.size) % K)])
     x = vals.reshape(-1, K)
     _check(x, bf16, f"exhaustive {'bf16' if bf16 else 'fp16'} {x.shape}")
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_every_absmax(bf16):
+    """Every finite FP16 / BF16 magnitude as a block's absmax (blocks
+    [a, -a/3, a/5, 0 ...]): the scale decision E4M3(absmax / 6) for every
+    input value, and the codes of a few quotients per block, byte for byte
+    against the oracle."""
+    if bf16:
+        a = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        a = np.arange(1, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    blocks = np.zeros((a.size, 16))
+    blocks[:, 0] = a
+    blocks[:, 1] = -a / 3
+    blocks[:, 2] = a / 5
+    K = 4096
+    vals = blocks.reshape(-1)
+    vals = np.concatenate([vals, np.zeros((-vals.size) % K)])
+    _check(vals.reshape(-1, K), bf16, f"every absmax {'bf16' if bf16 else 'fp16'}")
