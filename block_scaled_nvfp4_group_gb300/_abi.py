@@ -43,6 +43,13 @@ class SfRelayoutDesc(ctypes.Structure):
                 ("rows", ctypes.c_int), ("K", ctypes.c_int)]
 
 
+class StepDesc(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("SFA", ctypes.c_void_p),
+                ("SFB", ctypes.c_void_p), ("SFA_tiled", ctypes.c_void_p),
+                ("SFB_tiled", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
 # name -> (restype, argtypes); every symbol declared in the header
 SIGNATURES = {
     "nvfp4_group_gemm": (ctypes.c_int, [ctypes.POINTER(GroupDesc), ctypes.c_int, ctypes.c_void_p]),
@@ -58,6 +65,8 @@ SIGNATURES = {
     "nvfp4_sf_relayout_group": (ctypes.c_int, [ctypes.POINTER(SfRelayoutDesc), ctypes.c_int,
                                                ctypes.c_void_p]),
     "nvfp4_sf_tiled_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int]),
+    "nvfp4_relayout_and_gemm": (ctypes.c_int, [ctypes.POINTER(StepDesc), ctypes.c_int,
+                                               ctypes.POINTER(GemmEpilogue), ctypes.c_void_p]),
     "nvfp4_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p]),

@@ -100,6 +100,10 @@ struct GemmParams {
     float alpha[kMaxGroups];
     int out_bf16;              // C elements: 0 FP16, 1 BF16
     int swiglu;                // 1: every 256-column tile = 128 gate + 128 up columns, C is [M][N/2]
+    // 1: A and B were complete before the kernel preceding this launch in
+    // the stream began (the library's own relayout + GEMM call), so their
+    // loads need not wait for that kernel to finish
+    int early_ab;
     // stream-K launches: the flat sequence of (tile, k-stage) units, tiles in
     // list order, is cut into gridDim.x contiguous ranges, CTA c taking units
     // [c U / G, (c + 1) U / G) with U = units_total
@@ -683,8 +687,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = ptx::ld_shared_u32(tmem_slot);
     // With a programmatic launch the set-up above overlaps the previous
-    // kernel; nothing below touches global memory before that kernel is done.
-    ptx::grid_dependency_wait();
+    // kernel; nothing below touches global memory before that kernel is done,
+    // except the A and B loads of an early_ab launch (the previous kernel is
+    // then the library's scale relayout, which reads neither).
+    if (!(p.early_ab && (warp == kFirstLoaderWarp || warp == kFirstLoaderWarp + 1)))
+        ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};

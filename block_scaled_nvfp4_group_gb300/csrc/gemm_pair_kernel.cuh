@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = ptx::ld_shared_u32(tmem_slot);
-    ptx::grid_dependency_wait();
+    // the A and B loads of an early_ab launch do not wait for the previous
+    // kernel (the library's scale relayout, which reads neither)
+    if (!(p.early_ab && (warp == Cfg::kFirstLoader || warp == Cfg::kFirstLoader + 1)))
+        ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
     const WaitCtx wctx{abort_flag, p.err, p.timeout_ns};

@@ -315,7 +315,7 @@ int count_launches(const GroupDesc *groups, int num_groups, int bm, int bn)
 template <class ErrFn>
 int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
                     int sm_count, int kind, ErrFn err_for_launch, const GemmEpilogue *epi = nullptr,
-                    const SkScratch *sk = nullptr)
+                    const SkScratch *sk = nullptr, bool early_ab = false)
 {
     const bool swiglu = epi && epi->swiglu;
     const bool out_bf16 = epi && epi->out_bf16;
@@ -353,6 +353,7 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
             P.debug_drop_stage = drop;
             P.out_bf16 = out_bf16 ? 1 : 0;
             P.swiglu = swiglu ? 1 : 0;
+            P.early_ab = early_ab ? 1 : 0;
             if (ki.sk) {
                 P.sk_ws = sk->ws;
                 P.sk_flags = sk->flags;
@@ -469,6 +470,69 @@ extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, cons
     uint32_t *err = dev->err;
     return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; }, epi, &sk);
+}
+
+// ---------------------------------------------------------------------------
+// nvfp4_relayout_and_gemm: the scale relayout of every group and the grouped
+// GEMM as one call.  The GEMM follows the relayout in the stream with a
+// programmatic launch, and since the library launched that relayout itself
+// it knows A and B were complete before it began: the GEMM's A and B loads
+// start without waiting for the relayout to finish (early_ab); only the
+// scale loads, the MMAs and the epilogue wait for it.
+// ---------------------------------------------------------------------------
+extern "C" int nvfp4_relayout_and_gemm(const StepDesc *steps, int num_groups, const GemmEpilogue *epi,
+                                       cudaStream_t stream)
+{
+    using namespace nvfp4;
+    if (!steps || num_groups < 1)
+        return NVFP4_ERR_INVALID_ARGUMENT;
+    if (num_groups > kMaxGroupsPerCall)
+        return NVFP4_ERR_TOO_MANY;
+    static thread_local std::vector<GroupDesc> groups;
+    static thread_local std::vector<SfRelayoutDesc> rel;
+    groups.resize((size_t)num_groups);
+    rel.clear();
+    for (int i = 0; i < num_groups; ++i) {
+        const StepDesc &s = steps[i];
+        groups[i] = GroupDesc{s.A, s.B, s.SFA_tiled, s.SFB_tiled, s.C, s.M, s.N, s.K};
+        if (s.M > 0) {
+            if (!s.SFA || !s.SFB)
+                return NVFP4_ERR_INVALID_ARGUMENT;
+            if (!aligned16(s.SFA) || !aligned16(s.SFB))
+                return NVFP4_ERR_MISALIGNED;
+            rel.push_back(SfRelayoutDesc{s.SFA, s.SFA_tiled, s.M, s.K});
+            rel.push_back(SfRelayoutDesc{s.SFB, s.SFB_tiled, s.N, s.K});
+        }
+    }
+    int rc = validate_call(groups.data(), num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    const bool swiglu = epi && epi->swiglu;
+    if (swiglu)
+        for (int i = 0; i < num_groups; ++i)
+            if (groups[i].M > 0 && groups[i].N % 256 != 0)
+                return NVFP4_ERR_INVALID_ARGUMENT;
+    DeviceState *dev = nullptr;
+    rc = current_device(&dev);
+    if (rc != NVFP4_OK)
+        return rc;
+    int kind = choose_kind(groups.data(), num_groups, dev->sm_count, swiglu);
+    if (count_launches(groups.data(), num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+        return NVFP4_OK;
+    SkScratch sk{};
+    if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
+        kind = kKindWide;
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    rc = ensure_kernel_attributes(dev_id, kind);
+    if (rc != NVFP4_OK)
+        return rc;
+    rc = nvfp4_sf_relayout_group(rel.data(), (int)rel.size(), stream);
+    if (rc != NVFP4_OK)
+        return rc;
+    uint32_t *err = dev->err;
+    return plan_and_launch(groups.data(), num_groups, stream, dev_id, dev->sm_count, kind,
+                           [err](int) { return err; }, epi, &sk, true);
 }
 
 extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind,

@@ -21,7 +21,7 @@ class DeviceProblem:
     """A, B, row-major SFA/SFB, tiled SFA/SFB and C for every group.
 
     ``step()`` runs the whole path: one grouped relayout launch for every
-    SFA and SFB, then the grouped GEMM.  ``gemm()`` runs the GEMM alone on
+    SFA and SFB, then the grouped GEMM (nvfp4_relayout_and_gemm).  ``gemm()`` runs the GEMM alone on
     the tiled scales already produced."""
 
     def __init__(self, groups, device="cuda"):
@@ -72,6 +72,10 @@ class DeviceProblem:
         self.descs = ops.make_group_descs(
             (self.A[i], self.B[i], self.SFA_t[i], self.SFB_t[i], self.C[i], M, N, K)
             for i, (M, N, K) in enumerate(self.shapes))
+        self.step_descs = ops.make_step_descs(
+            (self.A[i], self.B[i], self.SFA[i], self.SFB[i], self.SFA_t[i], self.SFB_t[i], self.C[i],
+             M, N, K)
+            for i, (M, N, K) in enumerate(self.shapes))
 
     def relayout(self, stream=None) -> None:
         ops.sf_relayout_group(None, stream=stream, descs=self.relayout_descs)
@@ -80,8 +84,9 @@ class DeviceProblem:
         ops.group_gemm(None, stream=stream, descs=self.descs)
 
     def step(self, stream=None) -> None:
-        self.relayout(stream)
-        self.gemm(stream)
+        """The whole path in one library call (relayout, then the GEMM, whose
+        A and B loads need not wait for the relayout to finish)."""
+        ops.relayout_and_gemm(stream=stream, descs=self.step_descs)
 
     def outputs_fp16_bits(self):
         return [c.view(torch.int16).cpu().numpy().view(np.uint16) for c in self.C]

@@ -120,6 +120,43 @@ def group_gemm_ex(groups, alpha=None, out_bf16: bool = False, swiglu: bool = Fal
     del keep
 
 
+def make_step_descs(steps, out_bf16: bool = False, swiglu: bool = False):
+    """steps: iterable of (A, B, SFA, SFB, SFA_tiled, SFB_tiled, C, M, N, K)
+    device tensors, SFA / SFB the row-major scales [M, K/16] / [N, K/16]."""
+    steps = list(steps)
+    arr = (_abi.StepDesc * len(steps))()
+    checked = make_group_descs([(A, B, SFA_t, SFB_t, C, M, N, K)
+                                for (A, B, SFA, SFB, SFA_t, SFB_t, C, M, N, K) in steps],
+                               out_bf16=out_bf16, swiglu=swiglu)
+    for i, (A, B, SFA, SFB, SFA_t, SFB_t, C, M, N, K) in enumerate(steps):
+        if M > 0:
+            _check_u8(SFA, "SFA", M * K // 16)
+            _check_u8(SFB, "SFB", N * K // 16)
+        g = checked[i]
+        arr[i] = _abi.StepDesc(g.A, g.B, SFA.data_ptr() if M > 0 else None,
+                               SFB.data_ptr() if M > 0 else None, g.SFA, g.SFB, g.C, M, N, K)
+    return arr
+
+
+def relayout_and_gemm(steps=None, alpha=None, out_bf16: bool = False, swiglu: bool = False,
+                      stream=None, descs=None) -> None:
+    """The whole path of one grouped call (nvfp4_relayout_and_gemm): the
+    relayout of every SFA / SFB into the tiled buffers, then the grouped GEMM
+    (fused epilogue options as group_gemm_ex)."""
+    lib = _abi.load()
+    arr = descs if descs is not None else make_step_descs(steps, out_bf16=out_bf16, swiglu=swiglu)
+    epi = _abi.GemmEpilogue()
+    keep = None
+    if alpha is not None:
+        keep = (ctypes.c_float * len(arr))(*[float(a) for a in alpha])
+        epi.alpha = ctypes.cast(keep, ctypes.POINTER(ctypes.c_float))
+    epi.out_bf16 = 1 if out_bf16 else 0
+    epi.swiglu = 1 if swiglu else 0
+    _abi.check(lib.nvfp4_relayout_and_gemm(arr, len(arr), ctypes.byref(epi), _stream_handle(stream)),
+               "nvfp4_relayout_and_gemm")
+    del keep
+
+
 def group_gemm_plan(groups=None, descs=None):
     """(kind name, launches) nvfp4_group_gemm would use for these groups on
     the current device; nothing is launched."""

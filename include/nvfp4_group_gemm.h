@@ -201,6 +201,35 @@ typedef struct SfRelayoutDesc {
 } SfRelayoutDesc;
 int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t stream);
 
+/* The whole path of one grouped call: the scale relayout of every group's
+ * SFA and SFB (one nvfp4_sf_relayout_group launch) followed by the grouped
+ * GEMM of nvfp4_group_gemm_ex on the tiled scales.  Because the library
+ * launches the relayout itself, the GEMM's loads of A and B start while the
+ * relayout is still finishing (A and B must therefore be complete before
+ * this call's work begins in the stream, as for any stream-ordered call);
+ * its scale loads, MMAs and C stores wait for the relayout.
+ *  A, B, C, M, N, K  as in GroupDesc.
+ *  SFA, SFB          device, row-major E4M3FN scales [M][K/16], [N][K/16]
+ *                    (16-byte aligned; may be NULL when M == 0).
+ *  SFA_tiled,        device, nvfp4_sf_tiled_bytes(M, K) and
+ *  SFB_tiled           nvfp4_sf_tiled_bytes(N, K) bytes the relayout writes
+ *                    and the GEMM reads; owned by the caller.
+ * epi: NULL or the fused epilogue of nvfp4_group_gemm_ex.  Validation of
+ * every group precedes both launches; an error after the relayout launch
+ * (a CUDA launch failure) leaves the tiled scales written and C untouched. */
+typedef struct StepDesc {
+    const void *A;
+    const void *B;
+    const void *SFA;
+    const void *SFB;
+    void *SFA_tiled;
+    void *SFB_tiled;
+    void *C;
+    int M, N, K;
+} StepDesc;
+int nvfp4_relayout_and_gemm(const StepDesc *steps, int num_groups, const GemmEpilogue *epi,
+                            cudaStream_t stream);
+
 /* NVFP4 quantisation of a 16-bit float matrix into the GEMM's operand
  * format (the step that produces A or B; the pages take quantised data as
  * given, so this follows the generator of their "quantized" configuration:

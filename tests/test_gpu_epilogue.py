@@ -115,3 +115,43 @@ def test_swiglu_rejects_ragged_n():
     groups = workloads.make_groups([(64, 384, 256)], seed=55)
     with pytest.raises(_abi.Nvfp4Error):
         _run(groups, None, False, True)
+
+
+@pytest.mark.parametrize("kind", [None, "pair"])
+def test_relayout_and_gemm_fused(kind):
+    """The one-call path (nvfp4_relayout_and_gemm) from row-major scales, with
+    per-group scales, BF16 output and SwiGLU, against the oracle."""
+    from block_scaled_nvfp4_group_gb300 import ops, workloads
+    groups = workloads.make_groups(SHAPES, seed=54)
+    alpha = [1 / 64, 1 / 32, 1 / 128, 1 / 16]
+    steps = []
+    for g in groups:
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().reshape(-1)
+        C = torch.full((g.M, g.N // 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+        steps.append((dev(g.A), dev(g.B), dev(g.SFA), dev(g.SFB),
+                      torch.zeros(max(ops.sf_tiled_bytes(g.M, g.K), 16), dtype=torch.uint8, device="cuda"),
+                      torch.zeros(max(ops.sf_tiled_bytes(g.N, g.K), 16), dtype=torch.uint8, device="cuda"),
+                      C, g.M, g.N, g.K))
+    with gemm_env(kind):
+        ops.relayout_and_gemm(steps, alpha=alpha, out_bf16=True, swiglu=True)
+    torch.cuda.synchronize()
+    assert ops.last_device_error() == 0
+    o = oracle.get()
+    for i, (g, st) in enumerate(zip(groups, steps)):
+        got = st[6].view(torch.int16).cpu().numpy().view(np.uint16)
+        ref = o.gemm_ex(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, alpha=float(np.float32(alpha[i])),
+                        swiglu=True, bf16=True)
+        compare_bf16(got, ref, f"relayout+gemm group {i} kind={kind}")
+
+
+def test_relayout_and_gemm_rejects_before_launch():
+    """A missing row-major scale pointer is rejected before anything runs."""
+    from block_scaled_nvfp4_group_gb300 import _abi
+    lib = _abi.load()
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = buf.data_ptr()
+    arr = (_abi.StepDesc * 1)()
+    arr[0] = _abi.StepDesc(p, p, None, p, p, p, p, 128, 256, 256)
+    assert lib.nvfp4_relayout_and_gemm(arr, 1, None, None) == _abi.NVFP4_ERR_INVALID_ARGUMENT
+    arr[0] = _abi.StepDesc(p, p, p + 4, p, p, p, p, 128, 256, 256)
+    assert lib.nvfp4_relayout_and_gemm(arr, 1, None, None) == _abi.NVFP4_ERR_MISALIGNED
