@@ -43,6 +43,8 @@ def test_struct_layouts_match_header():
     # GroupDesc: 5 pointers + 3 ints (+ 4 bytes tail padding on LP64)
     assert ctypes.sizeof(_abi.GroupDesc) == 5 * 8 + 3 * 4 + 4
     assert ctypes.sizeof(_abi.SfRelayoutDesc) == 2 * 8 + 2 * 4
+    # StepDesc: 7 pointers + 3 ints (+ 4 bytes tail padding)
+    assert ctypes.sizeof(_abi.StepDesc) == 7 * 8 + 3 * 4 + 4
 
 
 def test_strerror_and_version(lib):
@@ -101,6 +103,30 @@ def test_relayout_rejects_before_launch(lib, args, code):
     assert lib.nvfp4_sf_relayout(*args, None) == code
     arr = (_abi.SfRelayoutDesc * 1)(_abi.SfRelayoutDesc(*args))
     assert lib.nvfp4_sf_relayout_group(arr, 1, None) == code
+
+
+P = 16   # a 16-byte-aligned stand-in address: validation never dereferences it
+
+
+def _step(a=P, sfa=P, **kw):
+    d = dict(A=a, B=P, SFA=sfa, SFB=P, SFA_tiled=P, SFB_tiled=P, C=P, M=128, N=256, K=256)
+    d.update(kw)
+    return _abi.StepDesc(d["A"], d["B"], d["SFA"], d["SFB"], d["SFA_tiled"], d["SFB_tiled"], d["C"],
+                         d["M"], d["N"], d["K"])
+
+
+@pytest.mark.parametrize("step,code", [
+    (_step(sfa=None), _abi.NVFP4_ERR_INVALID_ARGUMENT),          # no row-major scales
+    (_step(sfa=P + 4), _abi.NVFP4_ERR_MISALIGNED),
+    (_step(K=320), _abi.NVFP4_ERR_INVALID_ARGUMENT),             # K % 256 != 0
+    (_step(SFA_tiled=None), _abi.NVFP4_ERR_INVALID_ARGUMENT),    # no tiled buffer
+    (_step(a=P + 8), _abi.NVFP4_ERR_MISALIGNED),
+])
+def test_relayout_and_gemm_rejects_before_launch(lib, step, code):
+    arr = (_abi.StepDesc * 1)(step)
+    assert lib.nvfp4_relayout_and_gemm(arr, 1, None, None) == code
+    assert lib.nvfp4_relayout_and_gemm(None, 1, None, None) == _abi.NVFP4_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4_relayout_and_gemm(arr, 0, None, None) == _abi.NVFP4_ERR_INVALID_ARGUMENT
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
