@@ -205,3 +205,27 @@ def test_plan_picks_pairs_only_for_large_m():
     assert plan(workloads.make_groups([(300, 264, 256)], seed=1)) == ("stream", 1)
     shapes = [(64, 256, 256)] * 40
     assert plan(workloads.make_groups(shapes, seed=1)) == ("wide", 2)
+
+
+@pytest.mark.parametrize("shape", [(1, 1 << 20, 256), (1 << 20, 256, 256), (256, 256, 1 << 20)])
+def test_maximum_dimensions(shape):
+    """Each of M, N, K at the documented maximum (2^20): tile and stage
+    counts, relayout items and tensor-map coordinates at their largest;
+    sampled rows against the oracle (the 2^20-row case runs on CTA pairs)."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    groups = workloads.make_groups([shape], seed=91)
+    M, N, K = shape
+    if K == 1 << 20:
+        # an FP32 sum of 2^20 random products drifts past the tolerance the
+        # workloads' K <= 7168 are held to; keep 64 random 16-element scale
+        # blocks per row of A (the rest zero), so every K position is still
+        # loaded and addressed but each output sums ~1000 products, and a
+        # wrong K offset would move the non-zero blocks
+        rng = np.random.default_rng(92)
+        keep = np.zeros_like(groups[0].SFA)
+        for r in range(M):
+            idx = rng.choice(K // 16, size=64, replace=False)
+            keep[r, idx] = groups[0].SFA[r, idx]
+        groups[0].SFA[...] = keep
+    run_and_compare(groups, rows_per_group=4, seed=9)
+    torch.cuda.empty_cache()
