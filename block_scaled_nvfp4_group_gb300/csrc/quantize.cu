@@ -72,14 +72,20 @@ __device__ __forceinline__ float e4m3_value(uint32_t e)
     return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
-// E2M1 codes of (lo, hi) in bits 0..3 and 4..7
-__device__ __forceinline__ uint32_t e2m1x2_of(float lo, float hi)
+// E2M1 codes of eight values, value i in bits 4 i .. 4 i + 3 (four paired
+// conversions gathered into one word by a single vector move)
+__device__ __forceinline__ uint32_t e2m1x8_of(const float (&q)[8])
 {
     uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tmov.b32 %0, {t, 0, 0, 0};\n\t}"
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
         : "=r"(r)
-        : "f"(hi), "f"(lo));
-    return r & 0xFFu;
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return r;
 }
 
 // eight codes in a word: a zero magnitude loses its sign bit
@@ -166,18 +172,13 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
             uint32_t w = 0;
             if (sdec > 0.0f) {
                 const float r = rcp[sc];
+                float q[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float q[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float x = f[2 * i + h];
-                        const float q0 = x * r;
-                        q[h] = fmaf(fmaf(-q0, sdec, x), r, q0);
-                    }
-                    w |= e2m1x2_of(q[0], q[1]) << (8 * i);
+                for (int i = 0; i < 8; ++i) {
+                    const float q0 = f[i] * r;
+                    q[i] = fmaf(fmaf(-q0, sdec, f[i]), r, q0);
                 }
-                w = clear_negative_zeros(w);
+                w = clear_negative_zeros(e2m1x8_of(q));
             }
             if (in_k && row < p.rows)
                 *reinterpret_cast<uint32_t *>(p.codes + (size_t)row * (p.K / 2) + col / 2) = w;
