@@ -9,15 +9,17 @@
 // the 32 x 16-byte shape of one tcgen05.cp 32x128b.warpx4 (474067,
 // tcgen05_cp_nvfp4).  Rows past `rows` in the last block become zero.
 //
-// The relayout is a byte permutation, HBM-bound.  Persistent CTAs (four per
-// SM) walk the work items (one 128-row block x 64 scale columns = 16 atoms,
-// 8 KiB) round robin; each keeps four items in flight: a 2-D TMA load brings
-// the row-major tile into shared memory (rows past `rows` and columns past
-// K/16 read as zero), 256 threads transpose it (each 16-byte atom row is
-// four 4-byte words from rows q, q+32, q+64, q+96; the lane order makes the
-// shared-memory reads conflict-free) and write 32-byte runs of atoms to
-// global memory while the next tiles load.  Algorithmic traffic: rows * K/16
-// bytes read, the tiled size written.
+// The relayout is a byte permutation, HBM-bound, done entirely in
+// registers.  A warp takes 4 atom rows l (0..31) x 8 blocks of 16 scale
+// columns (4 atoms each) of one 128-row block: lane = 8 (l % 4) + block.
+// Each thread makes four 16-byte loads, rows l, l+32, l+64, l+96 of its
+// column block (a warp instruction reads four rows x 128 contiguous bytes),
+// transposes the 4 x 4 words in registers, and makes four 16-byte stores:
+// row l of each of its four atoms (a warp instruction writes eight atoms x
+// 64 contiguous bytes).  The warps of a CTA take neighbouring column groups
+// of the same rows.  Small CTAs with few registers keep the whole call's
+// loads in flight at once.  There is no shared memory and no wait to bound.
+// Algorithmic traffic: rows * K/16 bytes read, the tiled size written.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,134 +32,58 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kMaxDescs = 64;     // relayouts per launch (param block)
-constexpr int kChunkScales = 64;  // scale columns per item = 16 atoms
-constexpr int kThreads = 256;
-constexpr int kBufs = 4;          // items in flight per CTA
-constexpr int kTileBytes = 128 * kChunkScales;
-constexpr int kCtasPerSm = 4;
+constexpr int kThreads = 128;     // four warps, one work unit each
 constexpr int kMaxDim = 1 << 20;
 constexpr int kMaxCount = 4096;
 
 struct RelayoutParams {
-    CUtensorMap tm[kMaxDescs];   // uint8 {K/16, rows}, box {64, 128}, no swizzle
+    const uint8_t *src[kMaxDescs];
     uint8_t *dst[kMaxDescs];
+    int rows[kMaxDescs];
     int kcols[kMaxDescs];        // K / 16 scale columns per row
-    int chunks[kMaxDescs];       // ceil(kcols / 64)
-    int item_end[kMaxDescs];     // inclusive prefix sum of row blocks * chunks
+    int cgroups[kMaxDescs];      // groups of 128 scale columns per row: ceil(kcols / 128)
+    int unit_end[kMaxDescs];     // inclusive prefix sum of row blocks * 8 * cgroups
     int count;
-    int total_items;
-    uint32_t *err;
-    unsigned long long timeout_ns;
+    int total_units;
 };
-
-__device__ __forceinline__ void decode_item(const RelayoutParams &p, int item, int &d, int &rb, int &cc)
-{
-    d = 0;
-    while (item >= p.item_end[d])
-        ++d;
-    const int local = item - (d > 0 ? p.item_end[d - 1] : 0);
-    rb = local / p.chunks[d];
-    cc = local % p.chunks[d];
-}
 
 __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
 {
-    __shared__ __align__(128) uint8_t tile[kBufs][kTileBytes];
-    __shared__ __align__(8) uint64_t bars[kBufs];
-    __shared__ int ok_flag;
-    // programmatic launch: start early, but read and write global memory only
-    // once the previous kernel in the stream is done
+    // programmatic launch: read and write global memory only once the
+    // previous kernel in the stream is done
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
-
-    const uint32_t bar0 = ptx::smem_addr(&bars[0]);
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kBufs; ++b)
-            ptx::mbar_init(bar0 + 8u * b, 1);
-        ptx::fence_mbar_init();
-    }
-    __syncthreads();
-    const uint64_t pol = ptx::policy_evict_first();
-    uint32_t inflight = 0, inflight_parity = 0;    // thread 0's issued loads
-    auto issue = [&](int k) {
-        const int item = (int)blockIdx.x + k * (int)gridDim.x;
-        if (item >= p.total_items)
-            return;
-        int d, rb, cc;
-        decode_item(p, item, d, rb, cc);
-        const int b = k % kBufs;
-        const uint32_t bar = bar0 + 8u * b;
-        ptx::mbar_arrive_expect_tx(bar, kTileBytes);
-        ptx::tma_load_2d(ptx::smem_addr(&tile[b][0]), &p.tm[d], cc * kChunkScales, rb * 128, bar, pol);
-        inflight |= 1u << b;
-        inflight_parity = (inflight_parity & ~(1u << b)) | ((uint32_t)((k / kBufs) & 1) << b);
-    };
-    if (threadIdx.x == 0)
-        for (int k = 0; k < kBufs; ++k)
-            issue(k);
-
-    for (int k = 0;; ++k) {
-        const int item = (int)blockIdx.x + k * (int)gridDim.x;
-        if (item >= p.total_items)
-            break;
-        const int b = k % kBufs;
-        if (threadIdx.x == 0) {
-            // bounded wait for the tile; on expiry record it and stop (uniformly)
-            const uint32_t bar = bar0 + 8u * b, par = (uint32_t)((k / kBufs) & 1);
-            const uint64_t t0 = ptx::globaltimer_ns();
-            int ok = 1;
-            while (!ptx::mbar_try_wait(bar, par)) {
-                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-                    atomicOr(p.err, 1u);
-                    ok = 0;
-                    break;
-                }
-            }
-            if (ok)
-                inflight &= ~(1u << b);
-            ok_flag = ok;
-        }
-        __syncthreads();
-        if (!ok_flag)
-            break;
-        int d, rb, cc;
-        decode_item(p, item, d, rb, cc);
-        const int kcols = p.kcols[d];
-        const int natoms = min(16, (kcols - cc * kChunkScales) / 4);
-        const uint8_t *t = tile[b];
-        uint8_t *out = p.dst[d] + ((size_t)rb * (kcols / 4) + (size_t)cc * 16) * 512;
+    const int lane = threadIdx.x & 31;
+    const int unit = (int)blockIdx.x * (kThreads / 32) + (int)(threadIdx.x >> 5);
+    if (unit >= p.total_units)
+        return;
+    int d = 0;
+    while (unit >= p.unit_end[d])
+        ++d;
+    const int local = unit - (d > 0 ? p.unit_end[d - 1] : 0);
+    const int cgs = p.cgroups[d];
+    const int rb = local / (8 * cgs);
+    const int rem = local - rb * 8 * cgs;
+    const int lg = rem / cgs;                   // atom rows 4 lg .. 4 lg + 3
+    const int cg = rem - lg * cgs;              // column group (fastest: neighbouring warps)
+    const int l = 4 * lg + (lane >> 3);
+    const int cblk = 8 * cg + (lane & 7);      // block of 16 scale columns = atoms 4 cblk .. + 3
+    const int kcols = p.kcols[d];
+    if (cblk * 16 >= kcols)
+        return;
+    const int nrows = min(128, p.rows[d] - rb * 128);   // rows past it read as zero
+    const uint8_t *src = p.src[d] + (size_t)rb * 128 * kcols + (size_t)cblk * 16;
+    uint4 v[4];
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-            const int idx = threadIdx.x + kThreads * pass;     // 0..511
-            const int a = idx & 15;                            // atom
-            const int l = 2 * (idx >> 5) + ((idx >> 4) & 1);   // 16-byte row of the atom
-            if (a < natoms) {
-                uint4 y;
-                y.x = *reinterpret_cast<const uint32_t *>(t + (l)*kChunkScales + 4 * a);
-                y.y = *reinterpret_cast<const uint32_t *>(t + (l + 32) * kChunkScales + 4 * a);
-                y.z = *reinterpret_cast<const uint32_t *>(t + (l + 64) * kChunkScales + 4 * a);
-                y.w = *reinterpret_cast<const uint32_t *>(t + (l + 96) * kChunkScales + 4 * a);
-                *reinterpret_cast<uint4 *>(out + (size_t)a * 512 + l * 16) = y;
-            }
-        }
-        __syncthreads();    // tile[b] fully read before it is reloaded
-        if (threadIdx.x == 0)
-            issue(k + kBufs);
+    for (int q = 0; q < 4; ++q) {
+        const int r = l + 32 * q;
+        v[q] = r < nrows ? __ldg(reinterpret_cast<const uint4 *>(src + (size_t)r * kcols)) : make_uint4(0, 0, 0, 0);
     }
-    // loads issued but not consumed (after an expired wait) still write this
-    // CTA's shared memory: wait for them (bounded) before exiting
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kBufs; ++b) {
-            if (!(inflight & (1u << b)))
-                continue;
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar0 + 8u * b, (inflight_parity >> b) & 1u))
-                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-                    atomicOr(p.err, 2u);
-                    break;
-                }
-        }
-    }
+    uint8_t *o = p.dst[d] + ((size_t)rb * (kcols / 4) + (size_t)(4 * cblk)) * 512 + l * 16;
+    *reinterpret_cast<uint4 *>(o) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+    *reinterpret_cast<uint4 *>(o + 512) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+    *reinterpret_cast<uint4 *>(o + 1024) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+    *reinterpret_cast<uint4 *>(o + 1536) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
 }
 
 int validate(const SfRelayoutDesc &d)
@@ -206,12 +132,9 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
     auto launch = [&]() -> int {
         if (P.count == 0)
             return NVFP4_OK;
-        P.total_items = P.item_end[P.count - 1];
-        P.err = dev->err;
-        P.timeout_ns = wait_timeout_ns();
-        const int max_ctas = dev->sm_count * kCtasPerSm;
+        P.total_units = P.unit_end[P.count - 1];
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(P.total_items < max_ctas ? P.total_items : max_ctas);
+        cfg.gridDim = dim3((P.total_units + kThreads / 32 - 1) / (kThreads / 32));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
@@ -225,33 +148,30 @@ int nvfp4_sf_relayout_group(const SfRelayoutDesc *descs, int count, cudaStream_t
         return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
     };
     P.count = 0;
-    int items = 0;
+    int units = 0;
     for (int i = 0; i < count; ++i) {
         const SfRelayoutDesc &d = descs[i];
         if (d.rows == 0)
             continue;
         const int kcols = d.K / 16;
-        const int chunks = (kcols + kChunkScales - 1) / kChunkScales;
-        const int rblocks = (d.rows + 127) / 128;
-        const long long n = (long long)rblocks * chunks;
-        if (P.count == kMaxDescs || (long long)items + n > (1ll << 30)) {
+        const int cgroups = (kcols + 127) / 128;
+        const long long n = (long long)((d.rows + 127) / 128) * 8 * cgroups;
+        if (P.count == kMaxDescs || (long long)units + n > (1ll << 30)) {
             rc = launch();
             if (rc != NVFP4_OK)
                 return rc;
             P.count = 0;
-            items = 0;
+            units = 0;
         }
         const int j = P.count;
-        rc = encode_map_2d(&P.tm[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, d.src, (uint64_t)kcols,
-                           (uint64_t)d.rows, (uint64_t)kcols, kChunkScales, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (rc != NVFP4_OK)
-            return rc;
         P.count = j + 1;
+        P.src[j] = static_cast<const uint8_t *>(d.src);
         P.dst[j] = static_cast<uint8_t *>(d.dst);
+        P.rows[j] = d.rows;
         P.kcols[j] = kcols;
-        P.chunks[j] = chunks;
-        items += (int)n;
-        P.item_end[j] = items;
+        P.cgroups[j] = cgroups;
+        units += (int)n;
+        P.unit_end[j] = units;
     }
     return launch();
 }
