@@ -360,8 +360,12 @@ def run_ours(args):
     # contiguous pinned buffer) to the device, runs the step, and copies all
     # outputs back.  Two device problems of the same shapes take alternate
     # steps, so the host->device copy of step i+1 (its own stream) overlaps
-    # the compute and the device->host read of step i, as a server would.
-    probs = [prob, DeviceProblem(wl.groups, device=dev)]
+    # the compute and the device->host read of step i, as a server would --
+    # when the copies are large enough to outweigh the extra stream
+    # bookkeeping (>= 8 MiB of inputs per step); otherwise one problem and
+    # one stream, copies and step in sequence.
+    pipelined = int(prob.inputs.numel()) >= (8 << 20)
+    probs = [prob, DeviceProblem(wl.groups, device=dev) if pipelined else prob]
     h_in = torch.empty(prob.inputs.shape, dtype=torch.uint8, pin_memory=True)
     h_in.copy_(prob.inputs)
     h_out = [torch.empty(prob.outputs.shape, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
@@ -375,7 +379,12 @@ def run_ours(args):
     for e in ev_done + ev_out:
         e.record(stream)
 
-    def e2e_step(i):
+    def e2e_step_sequential(i):
+        prob.inputs.copy_(h_in, non_blocking=True)
+        prob.step()
+        h_out[0].copy_(prob.outputs, non_blocking=True)
+
+    def e2e_step_pipelined(i):
         b = i % 2
         p = probs[b]
         s_in.wait_event(ev_done[b])           # step i-2 has read its inputs
@@ -391,6 +400,7 @@ def run_ours(args):
             h_out[b].copy_(p.outputs, non_blocking=True)
             ev_out[b].record(s_out)
 
+    e2e_step = e2e_step_pipelined if pipelined else e2e_step_sequential
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -402,7 +412,8 @@ def run_ours(args):
     s_in.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step(i)
-    stream.wait_event(ev_out[(e2e_steps - 1) % 2])
+    if pipelined:
+        stream.wait_event(ev_out[(e2e_steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -453,7 +464,8 @@ def run_ours(args):
         "relayout": {"us": relayout_ms_mean * 1e3, "bytes": rl_bytes,
                      "gbs": rl_bytes / (relayout_ms_mean * 1e-3) / 1e9 if relayout_ms_mean > 0 else None},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "pipelined": pipelined},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
