@@ -33,7 +33,7 @@
 // kernelbot nvfp4-group-gemm submission 474067 (group_gemm_persistent_kernel,
 // tcgen05_mma_nvfp4, tcgen05_cp_nvfp4, the TMA producer warp); the split
 // loaders, the separate scale barrier, the store path, the bounded waits and
-// the tensor-memory budget are this build's own.
+// the tensor-memory budget are not taken from that page.
 //
 // Every mbarrier wait is bounded: when it expires the waiting role sets the
 // device error word and a shared abort flag, all roles leave their loops, the
