@@ -16,12 +16,12 @@
 //
 // One CTA of 128 threads takes a 128-row block and 128 columns (two scale
 // atoms; narrower tiles than a whole row leave a smaller last round of CTAs).
-// Warp w walks rows 32 w .. 32 w + 31, two rows per step: lane i loads
-// columns 8 (i % 16) .. + 7 of row 2 s + i / 16 (one 16-byte load; a warp
-// reads two 256-byte row pieces), eight steps in flight.  Lanes 2 j and
-// 2 j + 1 share 16-element block j (absmax through one shuffle), and the
-// lane's eight codes go out as one 4-byte store.  Scales are staged in shared memory in the
-// tiled atom layout (and row-major) and leave in 16-byte stores at the end.
+// Warp w walks rows 32 w .. 32 w + 31, four rows per step: lane i takes the
+// 16-element block i % 8 of row 4 s + i / 8 (two 16-byte loads; a warp reads
+// four 256-byte row pieces), four steps in flight, so every block's absmax,
+// scale and codes stay in one lane; its sixteen codes go out as one 8-byte
+// store.  Scales are staged in shared memory in the tiled atom layout (and
+// row-major) and leave in 16-byte stores at the end.
 // The quotients absmax / 6 and x / scale are formed as q = a r with r = 1 /
 // divisor correctly rounded (a constant, or a 128-entry shared-memory table
 // of __frcp_rn over the E4M3 codes, filled at block start beside the decoded
@@ -51,9 +51,9 @@ constexpr int kMaxDim = 1 << 20;
 constexpr int kRows = 128;       // rows per CTA (one scale row block)
 constexpr int kCols = 128;       // K elements per CTA (two scale atoms)
 constexpr int kThreads = 128;
-constexpr int kLanesPerRow = kCols / 8;
+constexpr int kLanesPerRow = kCols / 16;   // one lane per 16-element block
 constexpr int kRowsPerStep = 32 / kLanesPerRow;
-constexpr int kUnroll = 8;       // steps in flight per warp
+constexpr int kUnroll = 4;       // steps in flight per warp
 static_assert(kThreads == 128, "one thread per E4M3 code fills the scale tables");
 
 __device__ __forceinline__ uint32_t e4m3_of(float s)
@@ -140,53 +140,59 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
     const int c0 = blockIdx.x * kCols;          // first column of the tile
     const int rb = blockIdx.y;                  // 128-row block
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int piece = lane % kLanesPerRow;     // 8-column piece of the tile
+    const int j = lane % kLanesPerRow;         // 16-element block of the tile
     const int sub = lane / kLanesPerRow;        // row of the step
-    const int col = c0 + 8 * piece;             // this lane's first column
-    const bool in_k = col < p.K;                // K % 64 == 0: whole 8-column pieces
-    const int j = piece >> 1;                   // 16-element block of the tile
+    const int col = c0 + 16 * j;                // this lane's first column
+    const bool in_k = col < p.K;                // K % 64 == 0: whole blocks
     for (int rr = 0; rr < 32; rr += kUnroll * kRowsPerStep) {
-        uint4 v[kUnroll];
+        uint4 v[kUnroll][2];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int row = rb * kRows + warp * 32 + rr + u * kRowsPerStep + sub;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (in_k && row < p.rows)
-                v[u] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)row * p.K + col));
+            v[u][0] = make_uint4(0, 0, 0, 0);
+            v[u][1] = make_uint4(0, 0, 0, 0);
+            if (in_k && row < p.rows) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)row * p.K + col);
+                v[u][0] = __ldg(src);
+                v[u][1] = __ldg(src + 1);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int lr = warp * 32 + rr + u * kRowsPerStep + sub;   // row within the block
             const int row = rb * kRows + lr;
-            float f[8];
-            unpack8<BF16>(v[u], f);
+            float f[2][8];
+            unpack8<BF16>(v[u][0], f[0]);
+            unpack8<BF16>(v[u][1], f[1]);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                amax = fmaxf(amax, fabsf(f[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    amax = fmaxf(amax, fabsf(f[h][i]));
             constexpr float kSixth = 1.0f / 6.0f;
             const float a0 = amax * kSixth;
             const uint32_t sc = e4m3_of(fmaf(fmaf(-a0, 6.0f, amax), kSixth, a0));
             const float sdec = dec[sc];
-            uint32_t w = 0;
+            uint32_t w[2] = {0u, 0u};
             if (sdec > 0.0f) {
                 const float r = rcp[sc];
-                float q[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float q0 = f[i] * r;
-                    q[i] = fmaf(fmaf(-q0, sdec, f[i]), r, q0);
+                for (int h = 0; h < 2; ++h) {
+                    float q[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float q0 = f[h][i] * r;
+                        q[i] = fmaf(fmaf(-q0, sdec, f[h][i]), r, q0);
+                    }
+                    w[h] = clear_negative_zeros(e2m1x8_of(q));
                 }
-                w = clear_negative_zeros(e2m1x8_of(q));
             }
             if (in_k && row < p.rows)
-                *reinterpret_cast<uint32_t *>(p.codes + (size_t)row * (p.K / 2) + col / 2) = w;
-            if ((lane & 1) == 0) {
-                // rows past `rows` leave zero scales (amax 0)
-                atoms[j >> 2][(lr % 32) * 16 + (lr / 32) * 4 + (j & 3)] = (uint8_t)sc;
-                rm[lr][j] = (uint8_t)sc;
-            }
+                *reinterpret_cast<uint2 *>(p.codes + (size_t)row * (p.K / 2) + col / 2) = make_uint2(w[0], w[1]);
+            // rows past `rows` leave zero scales (amax 0)
+            atoms[j >> 2][(lr % 32) * 16 + (lr / 32) * 4 + (j & 3)] = (uint8_t)sc;
+            rm[lr][j] = (uint8_t)sc;
         }
     }
     __syncthreads();
