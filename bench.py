@@ -44,15 +44,15 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio, GB300
 # capture, keyed by workload, valid only for the kernel source it was taken
 # on (kernel_source_hash: the GEMM sources without comments).  From profiles/.
 NCU_TRAFFIC = {
-    "moe_gate_up": {"bytes": 140455168 + 7598592, "kernel_sha": "8634eb8f3688cb60",
+    "moe_gate_up": {"bytes": 140455168 + 7598592, "kernel_sha": "6199e7b6a1693649",
                     "source": "profiles/gemm_moe_gate_up.md"},
-    "moe_down": {"bytes": 68542720 + 4538112, "kernel_sha": "8634eb8f3688cb60",
+    "moe_down": {"bytes": 68542720 + 4538112, "kernel_sha": "6199e7b6a1693649",
                  "source": "profiles/gemm_moe_down.md"},
-    "quantized": {"bytes": 16568576 + 0, "kernel_sha": "8634eb8f3688cb60",
+    "quantized": {"bytes": 16568576 + 0, "kernel_sha": "6199e7b6a1693649",
                   "source": "profiles/gemm_quantized.md"},
-    "square": {"bytes": 75585536 + 92048128, "kernel_sha": "8634eb8f3688cb60",
+    "square": {"bytes": 75585536 + 92048128, "kernel_sha": "6199e7b6a1693649",
                "source": "profiles/gemm_square.md"},
-    "tiny": {"bytes": 156160 + 0, "kernel_sha": "8634eb8f3688cb60",
+    "tiny": {"bytes": 156160 + 0, "kernel_sha": "6199e7b6a1693649",
              "source": "profiles/gemm_tiny.md"},
 }
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "group_gemm.cu", "ptx.cuh")

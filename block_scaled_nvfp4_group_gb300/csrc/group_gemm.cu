@@ -220,7 +220,7 @@ int validate_call(const GroupDesc *groups, int num_groups)
 // 4096^3 groups), never for the small-M MoE shapes.  Stream-K (WIDE_SK) is
 // never chosen here: on GB300 it measured slower than whole tiles even where
 // it removes the most idle time (fewer tiles than SMs: 2 groups of 512 x
-// 3072 x 4096, 37.8 vs 21.0 us): its ranges start at scattered K offsets, so
+// 3072 x 4096, 33.7 vs 21.2 us): its ranges start at scattered K offsets, so
 // the first loads pull far more distinct bytes from HBM, each stage then
 // competes with 152 instead of 96 CTAs, and the cut tiles add a partial-sum
 // exchange.  NVFP4_GEMM_KIND overrides the choice.
@@ -535,6 +535,21 @@ extern "C" int nvfp4_relayout_and_gemm(const StepDesc *steps, int num_groups, co
                            [err](int) { return err; }, epi, &sk, true);
 }
 
+extern "C" int nvfp4_group_gemm_plan_for(const GroupDesc *groups, int num_groups, int sm_count,
+                                         int *kind, int *launches)
+{
+    using namespace nvfp4;
+    if (!kind || !launches || sm_count < 2)
+        return NVFP4_ERR_INVALID_ARGUMENT;
+    const int rc = validate_call(groups, num_groups);
+    if (rc != NVFP4_OK)
+        return rc;
+    const int k = choose_kind(groups, num_groups, sm_count);
+    *kind = k;
+    *launches = count_launches(groups, num_groups, kind_info(k).bm, kind_info(k).bn);
+    return NVFP4_OK;
+}
+
 extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind,
                                      int *launches)
 {
@@ -548,10 +563,7 @@ extern "C" int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, in
     rc = current_device(&dev);
     if (rc != NVFP4_OK)
         return rc;
-    const int k = choose_kind(groups, num_groups, dev->sm_count);
-    *kind = k;
-    *launches = count_launches(groups, num_groups, kind_info(k).bm, kind_info(k).bn);
-    return NVFP4_OK;
+    return nvfp4_group_gemm_plan_for(groups, num_groups, dev->sm_count, kind, launches);
 }
 
 // ---------------------------------------------------------------------------

@@ -168,6 +168,17 @@ def group_gemm_plan(groups=None, descs=None):
     return _abi.KIND_NAMES[kind.value], launches.value
 
 
+def group_gemm_plan_for(descs, sm_count: int):
+    """(kind name, launches) for a device with `sm_count` SMs, computed on the
+    host alone (no GPU needed); `descs` is a GroupDesc array."""
+    lib = _abi.load()
+    kind, launches = ctypes.c_int(-1), ctypes.c_int(0)
+    _abi.check(lib.nvfp4_group_gemm_plan_for(descs, len(descs), sm_count, ctypes.byref(kind),
+                                             ctypes.byref(launches)),
+               "nvfp4_group_gemm_plan_for")
+    return _abi.KIND_NAMES[kind.value], launches.value
+
+
 def quantize(x: torch.Tensor, codes: torch.Tensor | None = None, sf_tiled: torch.Tensor | None = None,
              sf_rowmajor: torch.Tensor | None = None, want_rowmajor: bool = False, stream=None):
     """NVFP4 quantisation of a [rows, K] float16 / bfloat16 CUDA tensor (see

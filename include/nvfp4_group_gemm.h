@@ -146,6 +146,16 @@ enum {
  * kind and launches: host pointers, written only on NVFP4_OK. */
 int nvfp4_group_gemm_plan(const GroupDesc *groups, int num_groups, int *kind, int *launches);
 
+/* The same plan for a device with sm_count SMs (152 on GB300), computed on
+ * the host alone: no CUDA call is made, so it also answers on a machine
+ * without a GPU.  The descriptors are validated like nvfp4_group_gemm's
+ * (their pointers are checked, never read).  NVFP4_GEMM_KIND applies as in
+ * nvfp4_group_gemm.  Returns NVFP4_ERR_INVALID_ARGUMENT for null kind or
+ * launches or sm_count < 2; kind and launches are written only on
+ * NVFP4_OK. */
+int nvfp4_group_gemm_plan_for(const GroupDesc *groups, int num_groups, int sm_count, int *kind,
+                              int *launches);
+
 /* The grouped GEMM of nvfp4_group_gemm for callers that are not allowed to
  * allocate device memory: engines and plugins that receive every byte of
  * device memory from an arena planned ahead and may not allocate while they

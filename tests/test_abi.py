@@ -132,3 +132,84 @@ def test_relayout_and_gemm_rejects_before_launch(lib, step, code):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         _abi.load(str(tmp_path / "missing.so"))
+
+
+# --- the host plan: kernel configuration and launch count, no GPU --------
+
+MOE_M = [366, 261, 336, 45, 223, 107, 317, 349]
+
+
+def _plan(lib, shapes, sm=152):
+    arr = (_abi.GroupDesc * len(shapes))(*[_desc(M=m, N=n, K=k) for m, n, k in shapes])
+    kind, launches = ctypes.c_int(-1), ctypes.c_int(-1)
+    rc = lib.nvfp4_group_gemm_plan_for(arr, len(arr), sm, ctypes.byref(kind), ctypes.byref(launches))
+    return rc, _abi.KIND_NAMES.get(kind.value), launches.value
+
+
+@pytest.mark.parametrize("shapes,sm,kind,launches", [
+    # small-M MoE shapes, every N a multiple of 256: 128 x 256 tiles
+    ([(m, 4096, 7168) for m in MOE_M], 152, "wide", 1),
+    ([(m, 7168, 2048) for m in MOE_M], 152, "wide", 1),
+    # 2048 tiles of 128 x 256 = 14 rounds of 152; 1024 pair tiles = 14 rounds of 76
+    ([(4096, 4096, 4096)] * 4, 152, "pair", 1),
+    # one round of tiles: no pairs ...
+    ([(512, 3072, 4096)] * 2, 152, "wide", 1),
+    # ... but 12 rounds on 8 SMs, and pairing adds none
+    ([(512, 3072, 4096)] * 2, 8, "pair", 1),
+    # 768 tiles = 6 rounds, 512 pair tiles = 7 rounds of 76: pairing would add one
+    ([(384, 4096, 256)] * 16, 152, "wide", 1),
+    ([(64, 256, 256), (128, 256, 256)], 152, "wide", 1),
+    # one N off the 256 grid sends the whole call to 128-column tiles
+    ([(77, 136, 512)], 152, "stream", 1),
+    ([(4096, 4096, 4096), (64, 136, 256)], 152, "stream", 1),
+    # 32 groups per launch; empty groups take no slot
+    ([(64, 256, 256)] * 32, 152, "wide", 1),
+    ([(64, 256, 256)] * 33, 152, "wide", 2),
+    ([(64, 256, 256)] * 65, 152, "wide", 3),
+    ([(0, 256, 256)] * 40 + [(64, 256, 256)] * 30, 152, "wide", 1),
+    ([(0, 256, 256)] * 3, 152, "wide", 0),
+])
+def test_plan_kind_and_launches(lib, monkeypatch, shapes, sm, kind, launches):
+    monkeypatch.delenv("NVFP4_GEMM_KIND", raising=False)
+    assert _plan(lib, shapes, sm) == (_abi.NVFP4_OK, kind, launches)
+
+
+@pytest.mark.parametrize("forced,shapes,kind", [
+    ("0", [(m, 4096, 7168) for m in MOE_M], "stream"),
+    ("7", [(m, 4096, 7168) for m in MOE_M], "wide_sk"),
+    ("6", [(m, 4096, 7168) for m in MOE_M], "pair"),
+    ("1", [(4096, 4096, 4096)] * 4, "wide"),
+    # a forced kind that cannot take the shapes falls back to 128-column tiles
+    ("1", [(77, 136, 512)], "stream"),
+    ("6", [(64, 128, 256)], "stream"),
+    ("7", [(77, 136, 512)], "stream"),
+    # out of range: ignored
+    ("99", [(4096, 4096, 4096)] * 4, "pair"),
+])
+def test_plan_forced_kind(lib, monkeypatch, forced, shapes, kind):
+    monkeypatch.setenv("NVFP4_GEMM_KIND", forced)
+    rc, k, n = _plan(lib, shapes)
+    assert (rc, k) == (_abi.NVFP4_OK, kind)
+    assert n == 1
+
+
+def test_plan_pair_launch_counts_256_row_tiles(lib, monkeypatch):
+    # launch splitting counts tiles of the chosen kind: 33 groups still need
+    # two launches with pair tiles
+    monkeypatch.setenv("NVFP4_GEMM_KIND", "6")
+    assert _plan(lib, [(512, 256, 256)] * 33) == (_abi.NVFP4_OK, "pair", 2)
+
+
+def test_plan_rejects_before_anything(lib):
+    kind, launches = ctypes.c_int(-5), ctypes.c_int(-5)
+    arr = (_abi.GroupDesc * 1)(_desc())
+    assert lib.nvfp4_group_gemm_plan_for(arr, 1, 1, ctypes.byref(kind), ctypes.byref(launches)) == \
+        _abi.NVFP4_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4_group_gemm_plan_for(arr, 1, 152, None, ctypes.byref(launches)) == \
+        _abi.NVFP4_ERR_INVALID_ARGUMENT
+    bad = (_abi.GroupDesc * 1)(_desc(K=100))
+    assert lib.nvfp4_group_gemm_plan_for(bad, 1, 152, ctypes.byref(kind), ctypes.byref(launches)) == \
+        _abi.NVFP4_ERR_INVALID_ARGUMENT
+    assert lib.nvfp4_group_gemm_plan_for(arr, 0, 152, ctypes.byref(kind), ctypes.byref(launches)) == \
+        _abi.NVFP4_ERR_INVALID_ARGUMENT
+    assert (kind.value, launches.value) == (-5, -5)     # written only on success
