@@ -495,6 +495,102 @@ def check_epilogue_mapping(o):
     assert np.count_nonzero(plain) == 4
 
 
+# --- quantisation decisions, exhaustive over the 16-bit input formats ---
+
+# the E2M1 magnitude grid's rounding boundaries (midpoints of neighbours) and
+# whether a value exactly on one goes up: ties go to the even code, i.e. up
+# at .75, 1.75 and 3.5, down at .25, 1.25, 2.5 and 5
+_E2M1_MIDS = [(0.25, False), (0.75, True), (1.25, False), (1.75, True), (2.5, False), (3.5, True),
+              (5.0, False)]
+
+
+def _finite_16bit(bf16: bool):
+    """(bits, float64 values) of every finite FP16 or BF16 number"""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        if bf16:
+            vals = (bits << 16).view(np.float32).astype(np.float64)
+        else:
+            vals = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    keep = np.isfinite(vals)
+    return bits[keep].astype(np.uint16), vals[keep]
+
+
+def _to_bits(v: np.ndarray, bf16: bool) -> np.ndarray:
+    if bf16:
+        return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    return v.astype(np.float16).view(np.uint16)
+
+
+def _e2m1_by_thresholds(x: np.ndarray, s: float) -> np.ndarray:
+    a = np.abs(x)
+    mag = np.zeros(x.shape, dtype=np.uint8)
+    for mid, tie_up in _E2M1_MIDS:
+        t = mid * s                      # <= 6 significant bits: exact in float64
+        mag += (a >= t) if tie_up else (a > t)
+    return np.where((x < 0) & (mag != 0), mag | 8, mag).astype(np.uint8)
+
+
+def check_quant_codes_exhaustive(o):
+    """Every finite FP16 and BF16 value x against every positive E4M3FN scale
+    s it can meet (|x| <= 6 s, in blocks whose absmax 6 s fixes the scale at
+    s): the oracle's code of x / s must be the rounding onto the magnitude
+    grid written as exact float64 comparisons of |x| with the grid's
+    midpoints times s.  With 11 or 8 significant bits, x / s is never within
+    half a single-precision ulp of a midpoint unless it is one, so taking the
+    quotient in single precision first changes no code; a single-precision
+    x * (1/s) does (it moves exact ties)."""
+    grid = torch_e4m3_table()
+    for bf16 in (False, True):
+        bits, vals = _finite_16bit(bf16)
+        for c in range(1, 0x7F):
+            s = float(grid[c])
+            xs = vals[np.abs(vals) <= 6.0 * s]
+            nblk = -(-xs.size // 15)
+            blocks = np.zeros((nblk, 16), dtype=np.float64)
+            blocks[:, 0] = 6.0 * s                               # absmax / 6 = s exactly
+            body = np.zeros(nblk * 15, dtype=np.float64)
+            body[:xs.size] = xs
+            blocks[:, 1:] = body.reshape(nblk, 15)
+            rows = -(-nblk // 64)
+            x = np.zeros((rows * 64, 16), dtype=np.float64)
+            x[:nblk] = blocks
+            codes, sf = o.quantize(_to_bits(x.reshape(rows, 64 * 16), bf16), rows, 64 * 16, bf16=bf16)
+            assert (sf.reshape(-1)[:nblk] == c).all(), ("scale", bf16, c)
+            got = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(rows * 64, 16)[:nblk]
+            want = _e2m1_by_thresholds(blocks, s)
+            bad = np.argwhere(got != want)
+            assert bad.size == 0, [("bf16" if bf16 else "fp16", s, float(blocks[i, j]), int(got[i, j]),
+                                    int(want[i, j])) for i, j in bad[:4]]
+
+
+def check_quant_scales_exhaustive(o):
+    """Every finite FP16 and BF16 value as a block's absmax: the oracle's scale
+    must be E4M3FN(absmax / 6) written as exact float64 comparisons of absmax
+    with six times the midpoints of neighbouring E4M3FN values (ties to the
+    even code, 448 for anything above it, 0 for zero)."""
+    grid = torch_e4m3_table()[:0x7F].astype(np.float64)    # codes 0..126, increasing
+    mids6 = 6.0 * (grid[1:] + grid[:-1]) / 2.0             # exact: few significant bits
+    for bf16 in (False, True):
+        bits, vals = _finite_16bit(bf16)
+        amax = np.abs(vals)
+        code = np.searchsorted(mids6, amax, side="left")    # midpoints strictly below amax
+        tie = np.isin(amax, mids6)
+        # on a midpoint between codes k and k+1 (code == k here): the even one
+        k = code[tie]
+        code[tie] = np.where(k % 2 == 0, k, k + 1)
+        code = np.minimum(code, 0x7E)
+        K = 1024
+        n = amax.size
+        rows = -(-n // (K // 16))
+        x = np.zeros(rows * (K // 16) * 16, dtype=np.float64)
+        x[0:n * 16:16] = vals
+        _, sf = o.quantize(_to_bits(x.reshape(rows, K), bf16), rows, K, bf16=bf16)
+        got = sf.reshape(-1)[:n]
+        bad = np.flatnonzero(got != code)
+        assert bad.size == 0, [(float(vals[i]), int(got[i]), int(code[i])) for i in bad[:4]]
+
+
 ALL_CHECKS = [
     check_e2m1_table, check_e4m3_all_codes, check_fp16_rounding, check_brute_force_tiny,
     check_brute_force_grouped, check_fixed_point, check_single_nonzero,
@@ -502,4 +598,5 @@ ALL_CHECKS = [
     check_signs, check_row_and_column_split, check_transpose_symmetry, check_relayout,
     check_quant_e4m3_vs_torch, check_quant_e2m1_rounding, check_quant_blocks,
     check_quant_vs_float64_generator, check_bf16_rounding, check_silu, check_epilogue_mapping,
+    check_quant_codes_exhaustive, check_quant_scales_exhaustive,
 ]

@@ -7,6 +7,13 @@ as element 2i for BOTH operands.  Two codes that share a byte always share a
 the terms of every dot product and leaves C unchanged; it is an equivalent
 mutant, not a mistake in what the oracle computes.  (It matters only for how
 callers pack bytes, which the check_nibble_order pin documents.)
+
+Likewise absent: the quantiser's scale quotient taken as amax * (1/6) in
+single precision.  check_quant_scales_exhaustive shows that it gives the same
+E4M3FN scale as amax / 6 for every finite FP16 and BF16 absmax (an exact tie
+m = amax / 6 on a midpoint stays within half an ulp of m), so it too is
+equivalent for these inputs.  The same slip in the element quotient,
+x * (1/s), is not: it moves exact E2M1 ties and is planted below.
 """
 import os
 
@@ -83,6 +90,9 @@ MUTANTS = {
         "        if (d < best_d || (d == best_d && (c & 1u) == 0 && (best & 1u) == 1)) {",
         "        const double d = fabs(x - nvfp4_oracle_e4m3fn(c));\n"
         "        if (nvfp4_oracle_e4m3fn(c) <= x) {"),
+    "quant_reciprocal_multiply": (
+        " / sdec)",
+        " * (1.0f / sdec))"),
     "swiglu_gate_up_swapped": (
         "const double g = alpha * acc[(size_t)m * N + 256 * j + c];\n"
         "                const double u = alpha * acc[(size_t)m * N + 256 * j + 128 + c];",
@@ -120,4 +130,5 @@ def test_mutant_is_caught(name, tmp_path):
             check(o)
         except (AssertionError, ValueError):
             failed.append(check.__name__)
+            break                       # one failing pin is enough
     assert failed, f"no pin caught the planted mistake {name}"
