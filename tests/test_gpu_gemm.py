@@ -190,6 +190,43 @@ def test_workload_square_sampled_rows(kind):
         run_and_compare(workloads.make_workload("square").groups, rows_per_group=24, seed=9)
 
 
+@pytest.mark.parametrize("kind", [None, "pair"])
+def test_step_graph_replays_new_inputs(kind):
+    """The step as bench.py times it: one nvfp4_relayout_and_gemm call (scale
+    relayout + grouped GEMM) captured as a CUDA graph on a side stream and
+    replayed, with new operand bytes and new row-major scales before every
+    replay; C is poisoned before each one."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+    shapes = [(256, 1024, 4096), (130, 512, 1024), (45, 2048, 2048)]
+    prob = DeviceProblem(workloads.make_groups(shapes, seed=81))
+    cap = torch.cuda.Stream()
+    with gemm_env(kind):
+        prob.step()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cap):
+            prob.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            prob.step()
+    o = oracle.get()
+    for rep in range(3):
+        groups = workloads.make_groups(shapes, seed=200 + rep)
+        for i, gr in enumerate(groups):
+            prob.A[i].copy_(torch.from_numpy(np.ascontiguousarray(gr.A).reshape(-1)))
+            prob.B[i].copy_(torch.from_numpy(np.ascontiguousarray(gr.B).reshape(-1)))
+            prob.SFA[i].copy_(torch.from_numpy(np.ascontiguousarray(gr.SFA).reshape(-1)))
+            prob.SFB[i].copy_(torch.from_numpy(np.ascontiguousarray(gr.SFB).reshape(-1)))
+        for c in prob.C:
+            c.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for gr, c in zip(groups, prob.outputs_fp16_bits()):
+            compare_fp16(c, o.gemm(gr.A, gr.SFA, gr.B, gr.SFB, gr.M, gr.N, gr.K), f"replay {rep}")
+
+
 def test_plan_picks_pairs_only_for_large_m():
     """The configuration the library picks per shape class: CTA pairs for
     the 4096^3 groups, 128 x 256 tiles for the small-M MoE shapes, 128 x 128
