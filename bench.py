@@ -189,10 +189,11 @@ def workload_config(wl) -> dict:
 # CPU oracle timing (reference arm and cpu_baseline)                          #
 # --------------------------------------------------------------------------- #
 
-def time_oracle(wl, budget_s: float):
+def time_oracle(wl, budget_s: float, keep: bool = False):
     """Time the oracle on an evenly spread sample of output rows of the
     workload, sized to take about `budget_s` seconds on all host cores.
-    Returns (TFLOPS, description, cores, seconds)."""
+    Returns (TFLOPS, description, cores, seconds, kept): kept is None, or
+    with keep=True the timed sample's results, [(group, rows, FP16 bits)]."""
     from oracle import oracle
     o = oracle.get()
     cores = os.cpu_count() or 1
@@ -210,21 +211,37 @@ def time_oracle(wl, budget_s: float):
     def sample(frac):
         t = time.perf_counter()
         done = nrows = 0
-        for g in wl.groups:
+        out = []
+        for i, g in enumerate(wl.groups):
+            if g.M == 0:
+                continue
             r = max(1, int(round(g.M * frac)))
-            rows = np.linspace(0, g.M - 1, r).astype(np.int64)
-            o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
-            done += 2 * r * g.N * g.K
-            nrows += r
-        return done, nrows, time.perf_counter() - t
+            rows = np.unique(np.linspace(0, g.M - 1, r).astype(np.int64))
+            ref = o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
+            if keep:
+                out.append((i, rows, ref))
+            done += 2 * rows.size * g.N * g.K
+            nrows += rows.size
+        return done, nrows, time.perf_counter() - t, out
 
-    done, nrows, dt = sample(frac)
+    done, nrows, dt, kept = sample(frac)
     if dt < 0.5 * budget_s and frac < 1.0:       # fixed per-group costs dominated: grow once
         frac = min(1.0, frac * budget_s / max(dt, 1e-3))
-        done, nrows, dt = sample(frac)
+        done, nrows, dt, kept = sample(frac)
     desc = (f"{nrows} of {sum(g.M for g in wl.groups)} output rows (all N columns) spread evenly "
             f"over the {len(wl.groups)} groups, {done / 1e9:.1f} GFLOP, {dt:.1f} s")
-    return done / dt / 1e12, desc, cores, dt
+    return done / dt / 1e12, desc, cores, dt, (kept if keep else None)
+
+
+def fp16_mismatches(got_bits: np.ndarray, ref_bits: np.ndarray) -> int:
+    """Elements outside |C - C_oracle| <= 1e-3 |C_oracle| + 1e-2 (non-finite
+    oracle values must be matched exactly)."""
+    g = got_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    fin = np.isfinite(r)
+    bad = int(np.count_nonzero(~(np.abs(g[fin] - r[fin]) <= 1e-3 * np.abs(r[fin]) + 1e-2)))
+    bad += int(np.count_nonzero(got_bits[~fin] != ref_bits[~fin]))
+    return bad
 
 
 def run_reference(args):
@@ -237,7 +254,7 @@ def run_reference(args):
     vals = []
     desc = cores = None
     for i in range(args.warmup + args.steps):
-        v, desc, cores, _ = time_oracle(wl, budget)
+        v, desc, cores, _, _ = time_oracle(wl, budget)
         if i >= args.warmup:
             vals.append(v)
     value = statistics.median(vals)
@@ -480,9 +497,23 @@ def run_ours(args):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        v, desc, cores, _ = time_oracle(wl, args.cpu_budget_s)
+        # the oracle's rows of this leg are also compared with the GPU's C
+        # of the last timed step (outside every timed region)
+        v, desc, cores, _, kept = time_oracle(wl, args.cpu_budget_s, keep=True)
+        try:
+            got = prob.outputs_fp16_bits()
+            n_el = n_bad = 0
+            for gi, rows, ref in kept:
+                n_el += ref.size
+                n_bad += fp16_mismatches(got[gi][rows], ref)
+            parity = {"elements": n_el, "mismatches": n_bad,
+                      "tolerance": "|C - C_oracle| <= 1e-3 |C_oracle| + 1e-2"}
+            if n_bad:
+                print(f"bench: {n_bad} of {n_el} sampled outputs differ from the oracle", file=sys.stderr)
+        except Exception as e:          # the check must not cost the measurement its line
+            parity = {"error": f"{type(e).__name__}: {e}"}
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "parity": parity}
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -41,3 +41,26 @@ def test_gpu_arm_fails_without_a_gpu():
     r = _run("--workload", "tiny", "--steps", "1", "--warmup", "3")
     assert r.returncode != 0
     assert not any(ln.lstrip().startswith("{") for ln in r.stdout.splitlines())
+
+
+def test_oracle_sample_and_parity_count():
+    """The CPU-baseline leg keeps the oracle rows it timed, and the bench's
+    mismatch count flags a planted error (CPU only: both sides here are the
+    oracle)."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_scaled_nvfp4_group_gb300 import workloads
+    wl = workloads.make_workload("tiny")
+    rate, desc, cores, dt, kept = bench.time_oracle(wl, 0.05, keep=True)
+    assert rate > 0 and cores >= 1
+    assert [gi for gi, _, _ in kept] == [0, 1]
+    for gi, rows, ref in kept:
+        g = wl.groups[gi]
+        assert ref.shape == (rows.size, g.N) and rows.min() >= 0 and rows.max() < g.M
+        assert bench.fp16_mismatches(ref, ref) == 0
+        worse = ref.copy()
+        v = worse.view(np.float16)
+        v[0, 0] = np.float16(float(v[0, 0]) + 1.0 + 0.01 * abs(float(v[0, 0])))
+        assert bench.fp16_mismatches(worse, ref) == 1
+    assert bench.time_oracle(wl, 0.05)[4] is None
