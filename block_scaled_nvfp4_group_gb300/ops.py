@@ -18,9 +18,17 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _check_u8(t: torch.Tensor, name: str, numel: int) -> None:
+def _check_device(t: torch.Tensor, name: str) -> None:
+    """The library works on the current CUDA device: every buffer it is
+    given must live there (a host or another GPU's pointer would fault)."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+
+
+def _check_u8(t: torch.Tensor, name: str, numel: int) -> None:
+    _check_device(t, name)
     if t.dtype not in (torch.uint8, torch.int8) and t.element_size() != 1:
         raise ValueError(f"{name} must hold bytes (uint8), got {t.dtype}")
     if not t.is_contiguous():
@@ -41,8 +49,10 @@ def sf_relayout(sf: torch.Tensor, rows: int, K: int, out: torch.Tensor | None = 
     nbytes = sf_tiled_bytes(rows, K)
     if out is None:
         out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=sf.device)
-    elif out.numel() < nbytes:
-        raise ValueError("out too small")
+    else:
+        _check_device(out, "out")
+        if out.numel() * out.element_size() < nbytes:
+            raise ValueError("out too small")
     _abi.check(lib.nvfp4_sf_relayout(ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                                      rows, K, _stream_handle(stream)), "nvfp4_sf_relayout")
     return out
@@ -54,7 +64,8 @@ def make_relayout_descs(items):
     arr = (_abi.SfRelayoutDesc * len(items))()
     for i, (src, dst, rows, K) in enumerate(items):
         _check_u8(src, "src", rows * K // 16)
-        if dst.numel() < sf_tiled_bytes(rows, K):
+        _check_device(dst, "dst")
+        if dst.numel() * dst.element_size() < sf_tiled_bytes(rows, K):
             raise ValueError("dst too small")
         arr[i] = _abi.SfRelayoutDesc(src.data_ptr(), dst.data_ptr(), rows, K)
     return arr
@@ -80,7 +91,11 @@ def make_group_descs(groups, out_bf16: bool = False, swiglu: bool = False):
         if M > 0:
             _check_u8(A, "A", M * K // 2)
             _check_u8(B, "B", N * K // 2)
-            if SFA.numel() < sf_tiled_bytes(M, K) or SFB.numel() < sf_tiled_bytes(N, K):
+            _check_device(SFA, "SFA (tiled)")
+            _check_device(SFB, "SFB (tiled)")
+            _check_device(C, "C")
+            if (SFA.numel() * SFA.element_size() < sf_tiled_bytes(M, K) or
+                    SFB.numel() * SFB.element_size() < sf_tiled_bytes(N, K)):
                 raise ValueError("scale buffers too small")
             want = torch.bfloat16 if out_bf16 else torch.float16
             n_out = N // 2 if swiglu else N
@@ -186,13 +201,22 @@ def quantize(x: torch.Tensor, codes: torch.Tensor | None = None, sf_tiled: torch
     row-major scales uint8 [rows, K/16] or None)."""
     if x.dtype not in (torch.float16, torch.bfloat16) or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D float16 or bfloat16 tensor")
+    _check_device(x, "x")
     rows, K = x.shape
     if codes is None:
         codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    else:
+        _check_u8(codes, "codes", rows * K // 2)
     if sf_tiled is None:
         sf_tiled = torch.empty(max(sf_tiled_bytes(rows, K), 16), dtype=torch.uint8, device=x.device)
+    else:
+        _check_device(sf_tiled, "sf_tiled")
+        if sf_tiled.numel() * sf_tiled.element_size() < sf_tiled_bytes(rows, K):
+            raise ValueError("sf_tiled too small")
     if sf_rowmajor is None and want_rowmajor:
         sf_rowmajor = torch.empty((rows, K // 16), dtype=torch.uint8, device=x.device)
+    elif sf_rowmajor is not None:
+        _check_u8(sf_rowmajor, "sf_rowmajor", rows * K // 16)
     lib = _abi.load()
     _abi.check(lib.nvfp4_quantize(x.data_ptr(), 1 if x.dtype == torch.bfloat16 else 0, rows, K,
                                   codes.data_ptr(), sf_tiled.data_ptr(),

@@ -213,3 +213,24 @@ def test_plan_rejects_before_anything(lib):
     assert lib.nvfp4_group_gemm_plan_for(arr, 0, 152, ctypes.byref(kind), ctypes.byref(launches)) == \
         _abi.NVFP4_ERR_INVALID_ARGUMENT
     assert (kind.value, launches.value) == (-5, -5)     # written only on success
+
+
+def test_binding_refuses_host_tensors(lib):
+    """The Python layer marshals device tensors only: host tensors are refused
+    before any library call, so nothing can run on a CPU copy."""
+    import torch
+    from block_scaled_nvfp4_group_gb300 import ops
+    M, N, K = 128, 256, 256
+    A = torch.zeros(M * K // 2, dtype=torch.uint8)
+    B = torch.zeros(N * K // 2, dtype=torch.uint8)
+    SFA = torch.zeros(ops.sf_tiled_bytes(M, K), dtype=torch.uint8)
+    SFB = torch.zeros(ops.sf_tiled_bytes(N, K), dtype=torch.uint8)
+    C = torch.zeros(M, N, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.make_group_descs([(A, B, SFA, SFB, C, M, N, K)])
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.make_relayout_descs([(torch.zeros(M * K // 16, dtype=torch.uint8), SFA, M, K)])
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.sf_relayout(torch.zeros(M * K // 16, dtype=torch.uint8), M, K)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.quantize(torch.zeros(M, K, dtype=torch.float16))
