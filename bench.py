@@ -2,20 +2,40 @@
 
 One step = the whole path over one grouped call: the scale-factor relayout
 of every SFA and SFB (one launch) and the grouped GEMM (one launch per 32
-groups), inputs resident in HBM, replayed as a captured CUDA graph.  The L2
-is flushed (a 512 MiB write) before every step, outside the timed events.
+groups), issued by one nvfp4_relayout_and_gemm call, inputs resident in HBM.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|NAME]
     python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+With no --workload every workload runs in one process and ONE JSON line is
+printed: its top level is the largest configuration (`square`, 4 groups of
+4096^3, the compute-bound case) and `per_config` holds the same figures for
+the other four (tiny, moe_gate_up, moe_down, quantized).
+
+Timing (per workload):
+* K steps are replayed back to back (a captured CUDA graph per step) and
+  bracketed by one pair of CUDA events; the inputs rotate over R resident
+  copies of the problem whose inputs total more than twice the L2, so each
+  step reads inputs that more than 2 x 129 MB of other data has passed
+  through L2 since their last use.  Workloads too small for that (tiny)
+  flush the L2 with a 512 MiB write before every step instead, outside the
+  events, and time each step alone.
+* The GEMM and the relayout are timed alone the same way (their own graphs,
+  K launches) for the roofline figures; `isolated` repeats both with an L2
+  flush and a pair of events around every single launch.
+* A sustained window (>= 1 s of the same step replays) follows, so that
+  nvidia-smi sees the GPU busy; its clocks are reported with the line.
 
 The `e2e` figure runs the same step through the public API from pinned host
 buffers: every step copies its inputs to the device and its outputs back,
 two device problems taking alternate steps so that one step's copies
 overlap the neighbouring step's compute.
 
-Prints one JSON line (rank 0).  Under torchrun each rank runs its own
-grouped call of the same shapes (weak scaling, no collective on the data
-path; the host reduces the step time with a max over ranks).
+Under torchrun (N ranks, one GPU each) the ranks share one global grouped
+call of N copies of the workload's group list, split by
+shard.shard_groups (expert parallel, no collective on the data path; the
+host reduces the step time with a max over ranks): each rank keeps about
+one workload's FLOPs (weak scaling).
 """
 from __future__ import annotations
 
@@ -38,7 +58,10 @@ import torch  # noqa: E402
 METRIC = "grouped-call TFLOPS and µs/call; achieved fraction of max(FLOP, HBM) roofline"
 UNIT = "TFLOPS"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25     # dense tensor-core ratio, GB300
+HEADLINE = "square"                     # the largest single-GPU configuration
+ORDER = ("tiny", "moe_gate_up", "moe_down", "quantized", "square")
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch from one ncu
 # capture, keyed by workload, valid only for the kernel source it was taken
@@ -122,22 +145,26 @@ class ClockSampler:
                 self.t.join(timeout=2)
 
     def summary(self, t0: float, t1: float) -> dict:
+        """Median SM clock, max clock and the throttle reasons seen between
+        wall times t0 and t1 (all samples if none fall inside)."""
         rows = [l.split(", ") for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.05]
         if not rows:
             rows = [l.split(", ") for (_, l) in self.lines]
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
                 sm.append(float(r[2]))
                 mx = float(r[3])
+                pw.append(float(r[4]))
                 for n, v in zip(names, r[6:10]):
                     if v.strip().lower() == "active":
                         reasons.add(n)
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
 
 
 def flops_of(shapes):
@@ -146,7 +173,7 @@ def flops_of(shapes):
 
 def bytes_of(shapes):
     return sum(M * K // 2 + N * K // 2 + M * K // 16 + N * K // 16 + M * N * 2
-               for M, N, K in shapes)
+               for M, N, K in shapes if M > 0)
 
 
 def relayout_bytes_of(shapes):
@@ -178,59 +205,78 @@ def barrier(ws: int):
         dist.barrier()
 
 
-def workload_config(wl) -> dict:
-    shapes = wl.shapes()
-    return {"workload": wl.name, "groups": len(shapes), "M_g": [s[0] for s in shapes],
-            "N": shapes[0][1], "K": shapes[0][2], "seed": wl.seed,
-            "l2": "flushed by a 512 MiB device write before every timed step"}
+def workload_config(name, groups, l2: str, ws: int = 1) -> dict:
+    shapes = [(g.M, g.N, g.K) for g in groups]
+    from block_scaled_nvfp4_group_gb300 import workloads
+    d = {"workload": name, "groups": len(shapes), "M_g": [s[0] for s in shapes],
+         "N": shapes[0][1], "K": shapes[0][2], "seed": workloads.describe(name)["seed"], "l2": l2}
+    if ws > 1:
+        d["parallelism"] = (f"expert parallel: {ws} ranks share one grouped call of {ws} copies of "
+                            f"the workload's groups (rank 0's groups listed)")
+    return d
 
 
 # --------------------------------------------------------------------------- #
 # CPU oracle timing (reference arm and cpu_baseline)                          #
 # --------------------------------------------------------------------------- #
 
-def time_oracle(wl, budget_s: float, keep: bool = False):
-    """Time the oracle on an evenly spread sample of output rows of the
-    workload, sized to take about `budget_s` seconds on all host cores.
-    Returns (TFLOPS, description, cores, seconds, kept): kept is None, or
-    with keep=True the timed sample's results, [(group, rows, FP16 bits)]."""
+def _groups_of(wl_or_groups):
+    return wl_or_groups.groups if hasattr(wl_or_groups, "groups") else list(wl_or_groups)
+
+
+def oracle_fraction(groups, budget_s: float) -> float:
+    """Fraction of every group's output rows the oracle covers in about
+    `budget_s` seconds on all host cores (calibrated on a few rows of the
+    first non-empty group)."""
     from oracle import oracle
     o = oracle.get()
     cores = os.cpu_count() or 1
-    g0 = wl.groups[0]
-    # calibration: a few rows of group 0
+    g0 = next(g for g in groups if g.M > 0)
     t = time.perf_counter()
-    o.gemm_rows(g0.A, g0.SFA, g0.B, g0.SFB, g0.M, g0.N, g0.K, list(range(min(cores, g0.M))))
+    n = min(cores, g0.M)
+    o.gemm_rows(g0.A, g0.SFA, g0.B, g0.SFB, g0.M, g0.N, g0.K, list(range(n)))
     cal = time.perf_counter() - t
-    per_row_flop = 2 * g0.N * g0.K
-    rate = min(cores, g0.M) * per_row_flop / max(cal, 1e-6)
-    target = rate * budget_s
-    total = flops_of(wl.shapes())
-    frac = min(1.0, target / total)
+    rate = n * 2 * g0.N * g0.K / max(cal, 1e-6)
+    total = flops_of([(g.M, g.N, g.K) for g in groups])
+    return min(1.0, rate * budget_s / total)
 
-    def sample(frac):
-        t = time.perf_counter()
-        done = nrows = 0
-        out = []
-        for i, g in enumerate(wl.groups):
-            if g.M == 0:
-                continue
-            r = max(1, int(round(g.M * frac)))
-            rows = np.unique(np.linspace(0, g.M - 1, r).astype(np.int64))
-            ref = o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
-            if keep:
-                out.append((i, rows, ref))
-            done += 2 * rows.size * g.N * g.K
-            nrows += rows.size
-        return done, nrows, time.perf_counter() - t, out
 
-    done, nrows, dt, kept = sample(frac)
+def oracle_sample(groups, frac: float, keep: bool = False):
+    """The oracle on an evenly spread `frac` of every group's output rows
+    (all N columns).  Returns (flops, rows, seconds, kept): kept is None, or
+    with keep=True the results, [(group index, rows, FP16 bits)]."""
+    from oracle import oracle
+    o = oracle.get()
+    t = time.perf_counter()
+    done = nrows = 0
+    out = []
+    for i, g in enumerate(groups):
+        if g.M == 0:
+            continue
+        r = max(1, int(round(g.M * frac)))
+        rows = np.unique(np.linspace(0, g.M - 1, r).astype(np.int64))
+        ref = o.gemm_rows(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, rows)
+        if keep:
+            out.append((i, rows, ref))
+        done += 2 * rows.size * g.N * g.K
+        nrows += rows.size
+    return done, nrows, time.perf_counter() - t, (out if keep else None)
+
+
+def time_oracle(wl_or_groups, budget_s: float, keep: bool = False):
+    """Time the oracle on an evenly spread sample of output rows, sized to
+    take about `budget_s` seconds on all host cores.  Returns (TFLOPS,
+    description, cores, seconds, kept) -- see oracle_sample for kept."""
+    groups = _groups_of(wl_or_groups)
+    cores = os.cpu_count() or 1
+    frac = oracle_fraction(groups, budget_s)
+    done, nrows, dt, kept = oracle_sample(groups, frac, keep)
     if dt < 0.5 * budget_s and frac < 1.0:       # fixed per-group costs dominated: grow once
         frac = min(1.0, frac * budget_s / max(dt, 1e-3))
-        done, nrows, dt, kept = sample(frac)
-    desc = (f"{nrows} of {sum(g.M for g in wl.groups)} output rows (all N columns) spread evenly "
-            f"over the {len(wl.groups)} groups, {done / 1e9:.1f} GFLOP, {dt:.1f} s")
-    return done / dt / 1e12, desc, cores, dt, (kept if keep else None)
+        done, nrows, dt, kept = oracle_sample(groups, frac, keep)
+    desc = (f"{nrows} of {sum(g.M for g in groups)} output rows (all N columns) spread evenly "
+            f"over the {len(groups)} groups, {done / 1e9:.1f} GFLOP, {dt:.1f} s")
+    return done / dt / 1e12, desc, cores, dt, kept
 
 
 def fp16_mismatches(got_bits: np.ndarray, ref_bits: np.ndarray) -> int:
@@ -245,25 +291,38 @@ def fp16_mismatches(got_bits: np.ndarray, ref_bits: np.ndarray) -> int:
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores, on
+    the headline workload (or --workload).  Every step (W untimed, then K
+    timed) is the oracle on the same bounded sample of the workload's output
+    rows, sized so the whole run takes about --ref-budget-s; ms_per_step is
+    the measured wall time of one such step and value its FLOPs / time.
+    Under torchrun only rank 0 runs."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     from block_scaled_nvfp4_group_gb300 import workloads
-    wl = workloads.make_workload(args.workload)
-    budget = max(1.0, args.ref_budget_s / max(1, args.steps + args.warmup))
-    vals = []
-    desc = cores = None
+    name = HEADLINE if args.workload == "all" else args.workload
+    groups = workloads.make_workload(name).groups
+    per_step = max(0.3, args.ref_budget_s / max(1, args.steps + args.warmup))
+    frac = oracle_fraction(groups, per_step)
+    secs, flops, nrows = [], 0, 0
     for i in range(args.warmup + args.steps):
-        v, desc, cores, _, _ = time_oracle(wl, budget)
+        done, nrows, dt, _ = oracle_sample(groups, frac)
         if i >= args.warmup:
-            vals.append(v)
-    value = statistics.median(vals)
-    shapes = wl.shapes()
+            secs.append(dt)
+            flops = done
+    ms_per_step = statistics.fmean(secs) * 1e3
+    value = flops / (ms_per_step * 1e-3) / 1e12
+    cores = os.cpu_count() or 1
+    desc = (f"every step: the oracle on {nrows} of {sum(g.M for g in groups)} output rows (all N "
+            f"columns) spread evenly over the {len(groups)} groups, {flops / 1e9:.2f} GFLOP; "
+            f"{cores} threads")
+    cfg = workload_config(name, groups, "host memory (CPU oracle)")
+    cfg["sample"] = desc
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": flops_of(shapes) / (value * 1e12) * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(wl),
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -274,128 +333,187 @@ def run_reference(args):
 # GPU arm                                                                     #
 # --------------------------------------------------------------------------- #
 
-def run_ours(args):
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+MAX_COPIES = 64
 
-    from block_scaled_nvfp4_group_gb300 import ops, workloads
-    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
 
-    wl = workloads.make_workload(args.workload)
-    if rank > 0:    # every rank its own batch of the same shapes
-        from block_scaled_nvfp4_group_gb300 import shard
-        wl = workloads.Workload(wl.name, wl.seed,
-                                workloads.make_groups(wl.shapes(),
-                                                      shard.rank_seed(wl.seed + 7919, rank)))
-    shapes = wl.shapes()
-    flops = flops_of(shapes)
-    gemm_bytes = bytes_of(shapes)
-    rl_bytes = relayout_bytes_of(shapes)
-    prob = DeviceProblem(wl.groups, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    from block_scaled_nvfp4_group_gb300 import _abi, ops
-    gemm_kind, gemm_launches = ops.group_gemm_plan(descs=prob.descs)
-    gemm_kernel = _abi.KIND_KERNELS[[k for k, v in _abi.KIND_NAMES.items() if v == gemm_kind][0]]
-    launches_per_step = 1 + gemm_launches
+def copies_needed(input_bytes: int) -> int:
+    """Resident copies of a problem so that between two uses of one copy's
+    inputs the other copies' inputs total at least 2 x L2; 0 when that would
+    take more than MAX_COPIES (the workload then flushes L2 instead)."""
+    r = 1 + -(-2 * L2_BYTES // max(1, input_bytes))
+    return r if r <= MAX_COPIES else 0
 
-    # warm-up (also JIT/driver first-use costs and the library's one-time
-    # per-device set-up, which must precede graph capture)
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        prob.step()
-    torch.cuda.synchronize()
 
-    # The step (and each of its two launches alone) captured as CUDA graphs:
-    # replays are back to back on the GPU, free of Python/host launch gaps.
-    # Captured on a stream that has run the step before: a stream's first
-    # stream-K GEMM allocates its scratch, which cannot happen during capture.
-    cap_stream = torch.cuda.Stream(dev)
-    with torch.cuda.stream(cap_stream):
-        prob.step()
-    torch.cuda.synchronize()
+class Timer:
+    """CUDA events on one stream."""
 
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream):
-            fn()
-        return g
-    g_step = capture(prob.step)
-    g_rel = capture(prob.relayout)
-    g_gemm = capture(prob.gemm)
-    for _ in range(3):
-        flush.zero_()
-        g_step.replay()
-    torch.cuda.synchronize()
+    def __init__(self, stream):
+        self.stream = stream
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.15)
+    def span(self, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        fn()
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
 
-    def timed(graph, n):
+    def each(self, fn, n, pre):
+        """n launches of fn, each after pre() and bracketed by its own events;
+        mean and median in ms"""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for a, b in evs:
-            flush.zero_()
-            a.record(stream)
-            graph.replay()
-            b.record(stream)
-        return evs
+            pre()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        t = [a.elapsed_time(b) for a, b in evs]
+        return statistics.fmean(t), statistics.median(t)
 
-    # ---- timed: K whole steps (events around each, L2 flushed in between)
+
+def capture(fns, stream):
+    """One CUDA graph running fns in order (launches issued by the library
+    keep their programmatic dependent launch edges inside the graph)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in fns:
+            f()
+    return g
+
+
+def measure_workload(name, groups, args, dev, ws, sampler):
+    """Every figure of one workload on this rank (see the module docstring)."""
+    from block_scaled_nvfp4_group_gb300 import _abi, ops
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+
+    shapes = [(g.M, g.N, g.K) for g in groups]
+    flops, gemm_bytes, rl_bytes = flops_of(shapes), bytes_of(shapes), relayout_bytes_of(shapes)
+    stream = torch.cuda.current_stream(dev)
+    timer = Timer(stream)
+    first = DeviceProblem(groups, device=dev)
+    R = copies_needed(int(first.inputs.numel()))
+    probs = [first] + [DeviceProblem(groups, device=dev) for _ in range(max(R, 2) - 1)]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if R == 0 else None
+    if R:
+        l2 = (f"inputs rotate over {R} resident copies ({R * int(first.inputs.numel()) / 1e6:.0f} MB "
+              f"of inputs): between two uses of a copy > 2 x L2 of other inputs pass through; "
+              f"steps back to back")
+    else:
+        l2 = "flushed by a 512 MiB device write before every timed step (outside the events)"
+    kind, gemm_launches = ops.group_gemm_plan(descs=first.descs)
+    kernel = _abi.KIND_KERNELS[[k for k, v in _abi.KIND_NAMES.items() if v == kind][0]]
+    per_step = 1 + gemm_launches
+
+    def pre():
+        if flush is not None:
+            flush.zero_()
+
+    # warm-up: first-use costs and the library's one-time per-device set-up
+    # (which must precede graph capture); every copy's tiled scales exist
+    # afterwards, so the GEMM can also run alone
+    for _ in range(max(args.warmup, 3)):
+        for p in probs:
+            pre()
+            p.step()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.stream(cap):
+        probs[0].step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    seq = [probs[i % len(probs)] for i in range(K)] if R else [probs[0]] * K
+
+    def graph_of(method):
+        if R:
+            return capture([getattr(p, method) for p in seq], cap)
+        return capture([getattr(probs[0], method)], cap)
+
+    g_step, g_gemm, g_rel = graph_of("step"), graph_of("gemm"), graph_of("relayout")
+    for g in (g_step, g_gemm, g_rel):
+        pre()
+        g.replay()
+    torch.cuda.synchronize()
+
+    def run_k(g):
+        """ms per launch over exactly K launches"""
+        if R:
+            return timer.span(g.replay) / K, None
+        return timer.each(g.replay, K, pre)
+
+    # ---- the timed region: exactly K steps
     barrier(ws)
     torch.cuda.synchronize()
     w0 = time.time()
-    ev = timed(g_step, args.steps)
+    step_ms, _ = run_k(g_step)
     torch.cuda.synchronize()
     barrier(ws)
+    step_ms = max_over_ranks(step_ms, ws)
+    gemm_ms, _ = run_k(g_gemm)
+    rel_ms, _ = run_k(g_rel)
+    # sustained window: the same K-step replays for >= --sustain-s
+    s0 = time.time()
+    n_sus = 0
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream)
+    batch = max(1, min(8, int(0.05 / max(step_ms * 1e-3 * (K if R else 1), 1e-6))))
+    while time.time() - s0 < args.sustain_s:
+        for _ in range(batch):
+            pre()
+            g_step.replay()
+        n_sus += batch
+        torch.cuda.synchronize()      # the host waits for every batch: replays are asynchronous
+    ev_b.record(stream)
+    torch.cuda.synchronize()
     w1 = time.time()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(sum(step_ms), ws)
-    ms_per_step = total_ms / args.steps
-    # the two launches alone (same protocol) for the per-kernel figures
-    n_part = min(args.steps, 300)
-    ev_g = timed(g_gemm, n_part)
-    ev_r = timed(g_rel, n_part)
-    torch.cuda.synchronize()
-    # per-launch durations: the mean (the events tick in ~1 us steps, so the
-    # median jumps between neighbouring steps; the mean does not)
-    gemm_t = [a.elapsed_time(b) for a, b in ev_g]
-    rel_t = [a.elapsed_time(b) for a, b in ev_r]
-    gemm_ms_med, relayout_ms_med = statistics.median(gemm_t), statistics.median(rel_t)
-    gemm_ms_mean, relayout_ms_mean = statistics.fmean(gemm_t), statistics.fmean(rel_t)
-    # eager (no graph) step time, for reference
-    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n_part)]
-    for a, b in ev_e:
-        flush.zero_()
-        a.record(stream)
-        prob.step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    eager_ms_med = statistics.median([a.elapsed_time(b) for a, b in ev_e])
+    # (with per-step flushes the window also holds the flush writes)
+    sus_ms = ev_a.elapsed_time(ev_b) / (n_sus * K) if R else None
+    # isolated launches: L2 flushed before each, events around each
+    iso_flush = flush if flush is not None else torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_iso = min(K, 100)
+    one = probs[0]
+    iso_gemm = timer.each(one.gemm, n_iso, iso_flush.zero_)
+    iso_rel = timer.each(one.relayout, n_iso, iso_flush.zero_)
+    iso_step = timer.each(one.step, n_iso, iso_flush.zero_)
+    del iso_flush
+    clocks = sampler.summary(w0, w1)
+    rc = ops.last_device_error()
+    if rc != 0:
+        raise RuntimeError(f"{name}: device error word {rc} after the timed launches")
+    rec = {
+        "name": name, "shapes": shapes, "groups": groups, "probs": probs, "flops": flops,
+        "gemm_bytes": gemm_bytes, "rl_bytes": rl_bytes, "l2": l2, "copies": R,
+        "kind": kind, "kernel": kernel, "launches_per_step": per_step,
+        "step_ms": step_ms, "gemm_ms": gemm_ms, "rel_ms": rel_ms,
+        "sustained": {"steps": n_sus * (K if R else 1), "ms_per_step": sus_ms,
+                      "seconds": round(w1 - s0, 2)},
+        "isolated_us": {"step_mean": iso_step[0] * 1e3, "gemm_mean": iso_gemm[0] * 1e3,
+                        "gemm_median": iso_gemm[1] * 1e3, "relayout_mean": iso_rel[0] * 1e3},
+        "clocks": clocks,
+    }
+    del g_step, g_gemm, g_rel
+    return rec
 
-    # ---- end to end through the public API with host buffers: every step
-    # copies all inputs (A, B and the row-major scales of every group, one
-    # contiguous pinned buffer) to the device, runs the step, and copies all
-    # outputs back.  Two device problems of the same shapes take alternate
-    # steps, so the host->device copy of step i+1 (its own stream) overlaps
-    # the compute and the device->host read of step i, as a server would --
-    # when the copies are large enough to outweigh the extra stream
-    # bookkeeping (>= 8 MiB of inputs per step); otherwise one problem and
-    # one stream, copies and step in sequence.
+
+def measure_e2e(rec, args, dev, ws):
+    """The step through the public API with host buffers: every step copies
+    all inputs (A, B and the row-major scales of every group: one pinned
+    buffer) to the device, runs the step and copies all outputs back.  Two
+    device problems take alternate steps, so the host->device copy of step
+    i+1 (its own stream) overlaps the compute and the device->host read of
+    step i, when a step moves >= 8 MiB of inputs; otherwise one problem and
+    copies and step in sequence."""
+    probs = rec["probs"]
+    stream = torch.cuda.current_stream(dev)
+    prob = probs[0]
     pipelined = int(prob.inputs.numel()) >= (8 << 20)
-    probs = [prob, DeviceProblem(wl.groups, device=dev) if pipelined else prob]
+    pair = [probs[0], probs[1]] if pipelined else [prob, prob]
     h_in = torch.empty(prob.inputs.shape, dtype=torch.uint8, pin_memory=True)
     h_in.copy_(prob.inputs)
     h_out = [torch.empty(prob.outputs.shape, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
-    h2d = int(prob.inputs.numel())
-    d2h = int(prob.outputs.numel())
-    e2e_steps = max(3, min(args.steps, 50))
+    n = max(3, min(args.steps, 50))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -403,14 +521,14 @@ def run_ours(args):
     for e in ev_done + ev_out:
         e.record(stream)
 
-    def e2e_step_sequential(i):
+    def sequential(i):
         prob.inputs.copy_(h_in, non_blocking=True)
         prob.step()
         h_out[0].copy_(prob.outputs, non_blocking=True)
 
-    def e2e_step_pipelined(i):
+    def overlapped(i):
         b = i % 2
-        p = probs[b]
+        p = pair[b]
         s_in.wait_event(ev_done[b])           # step i-2 has read its inputs
         with torch.cuda.stream(s_in):
             p.inputs.copy_(h_in, non_blocking=True)
@@ -424,102 +542,153 @@ def run_ours(args):
             h_out[b].copy_(p.outputs, non_blocking=True)
             ev_out[b].record(s_out)
 
-    e2e_step = e2e_step_pipelined if pipelined else e2e_step_sequential
+    step = overlapped if pipelined else sequential
     for i in range(2):
-        e2e_step(i)
+        step(i)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     e0.record(stream)
     s_in.wait_event(e0)
-    for i in range(e2e_steps):
-        e2e_step(i)
+    for i in range(n):
+        step(i)
     if pipelined:
-        stream.wait_event(ev_out[(e2e_steps - 1) % 2])
+        stream.wait_event(ev_out[(n - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / e2e_steps
-    sampler.stop()
-    clocks = sampler.summary(w0, w1)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws) / n
+    return {"value": ws * rec["flops"] / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(prob.inputs.numel()), "d2h_bytes_per_step": int(prob.outputs.numel()),
+            "ms_per_step": ms, "steps": n, "pipelined": pipelined}
 
-    if rank != 0:
-        return
 
-    peaks = load_peaks()
+def roofline_of(rec, peaks):
+    """The GEMM against max(bytes / HBM, FLOPs / FP4 peak): HBM-bound
+    workloads report algorithmic bytes per launch / mean launch time against
+    the measured copy bandwidth, tensor-bound ones FLOPs / time against the
+    measured bf16 peak x the nominal FP4 / bf16 ratio."""
     fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-    t_mem = gemm_bytes / (peaks["hbm_gbs"] * 1e9)
-    t_flop = flops / (fp4_peak * 1e12)
+    t_mem = rec["gemm_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flop = rec["flops"] / (fp4_peak * 1e12)
     bound = "hbm" if t_mem >= t_flop else "tensor"
-    gemm_s = gemm_ms_mean * 1e-3
+    gemm_s = rec["gemm_ms"] * 1e-3 / max(1, rec["launches_per_step"] - 1)
     if bound == "hbm":
-        achieved = gemm_bytes / gemm_s / 1e9
-        peak, unit = peaks["hbm_gbs"], "GB/s"
+        achieved, peak, unit = rec["gemm_bytes"] / gemm_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
-        achieved = flops / gemm_s / 1e12
-        peak, unit = fp4_peak, "TFLOP/s"
+        achieved, peak, unit = rec["flops"] / gemm_s / 1e12, fp4_peak, "TFLOP/s"
     traffic = None
-    rec = NCU_TRAFFIC.get(args.workload)
-    if rec and rec.get("kernel_sha") == kernel_source_hash():
-        traffic = rec["bytes"]
+    ncu = NCU_TRAFFIC.get(rec["name"])
+    if ncu and ncu.get("kernel_sha") == kernel_source_hash():
+        traffic = ncu["bytes"]
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "kernel": rec["kernel"], "kernel_config": rec["kind"],
+            "peak_source": peaks["source"] + (" (hbm_gbs)" if bound == "hbm" else
+                                              " (bf16_tflops x 6, nominal fp4/bf16 dense ratio)"),
+            "algorithmic_bytes_per_launch": rec["gemm_bytes"], "flops_per_launch": rec["flops"],
+            "launch_us": gemm_s * 1e6,
+            "roofline_fraction_of_max_time": max(t_mem, t_flop) / gemm_s}
 
-    value = ws * flops / (ms_per_step * 1e-3) / 1e12
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
-        "config": workload_config(wl),
-        "us_per_call": {"step": ms_per_step * 1e3, "gemm_mean": gemm_ms_mean * 1e3,
-                        "gemm_median": gemm_ms_med * 1e3, "relayout_mean": relayout_ms_mean * 1e3,
-                        "relayout_median": relayout_ms_med * 1e3,
-                        "step_eager_median": eager_ms_med * 1e3},
-        "launch": "each step replayed as a captured CUDA graph (relayout + GEMM launches)",
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": gemm_kernel, "kernel_config": gemm_kind,
-                     "peak_source": peaks["source"] + (
-                         " (hbm_gbs)" if bound == "hbm" else
-                         " (bf16_tflops x 6, nominal fp4/bf16 dense ratio)"),
-                     "algorithmic_bytes_per_launch": gemm_bytes,
-                     "flops_per_launch": flops,
-                     "roofline_fraction_of_max_time": max(t_mem, t_flop) / gemm_s},
-        "relayout": {"us": relayout_ms_mean * 1e3, "bytes": rl_bytes,
-                     "gbs": rl_bytes / (relayout_ms_mean * 1e-3) / 1e9 if relayout_ms_mean > 0 else None,
-                     "peak_gbs": peaks["hbm_gbs"],
-                     "frac": (rl_bytes / (relayout_ms_mean * 1e-3) / 1e9 / peaks["hbm_gbs"]
-                              if relayout_ms_mean > 0 else None)},
-        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "pipelined": pipelined},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-    }
-    if not args.no_cpu_baseline:
-        # the oracle's rows of this leg are also compared with the GPU's C
-        # of the last timed step (outside every timed region)
-        v, desc, cores, _, kept = time_oracle(wl, args.cpu_budget_s, keep=True)
-        try:
-            got = prob.outputs_fp16_bits()
-            n_el = n_bad = 0
+
+def oracle_check(rec, budget_s):
+    """The oracle on a sample of output rows (timed: the CPU baseline) and
+    the same rows of the GPU's C in every resident copy (element by element,
+    outside every timed region)."""
+    v, desc, cores, _, kept = time_oracle(rec["groups"], budget_s, keep=True)
+    n_el = n_bad = 0
+    try:
+        for p in rec["probs"]:
+            got = p.outputs_fp16_bits()
             for gi, rows, ref in kept:
                 n_el += ref.size
                 n_bad += fp16_mismatches(got[gi][rows], ref)
-            parity = {"elements": n_el, "mismatches": n_bad,
-                      "tolerance": "|C - C_oracle| <= 1e-3 |C_oracle| + 1e-2"}
-            if n_bad:
-                print(f"bench: {n_bad} of {n_el} sampled outputs differ from the oracle", file=sys.stderr)
-        except Exception as e:          # the check must not cost the measurement its line
-            parity = {"error": f"{type(e).__name__}: {e}"}
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc, "parity": parity}
-    print(json.dumps(line), flush=True)
+        parity = {"elements": n_el, "mismatches": n_bad, "copies_checked": len(rec["probs"]),
+                  "tolerance": "|C - C_oracle| <= 1e-3 |C_oracle| + 1e-2"}
+        if n_bad:
+            print(f"bench: {rec['name']}: {n_bad} of {n_el} sampled outputs differ from the oracle",
+                  file=sys.stderr)
+    except Exception as e:          # the check must not cost the measurement its line
+        parity = {"error": f"{type(e).__name__}: {e}"}
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}, parity
+
+
+def summary_of(rec, args, ws, peaks):
+    K = args.steps
+    return {
+        "value": ws * rec["flops"] / (rec["step_ms"] * 1e-3) / 1e12,
+        "ms_per_step": rec["step_ms"],
+        "config": workload_config(rec["name"], rec["groups"], rec["l2"], ws),
+        "us_per_call": {"step": rec["step_ms"] * 1e3,
+                        "gemm": rec["gemm_ms"] * 1e3 / max(1, rec["launches_per_step"] - 1),
+                        "relayout": rec["rel_ms"] * 1e3},
+        "isolated_us": rec["isolated_us"],
+        "roofline": roofline_of(rec, peaks),
+        "relayout": {"us": rec["rel_ms"] * 1e3, "bytes": rec["rl_bytes"],
+                     "gbs": rec["rl_bytes"] / (rec["rel_ms"] * 1e-3) / 1e9,
+                     "peak_gbs": peaks["hbm_gbs"],
+                     "frac": rec["rl_bytes"] / (rec["rel_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "sustained": rec["sustained"],
+        "gpu_launches": rec["launches_per_step"] * K,
+        "clocks": rec["clocks"],
+    }
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_scaled_nvfp4_group_gb300 import workloads
+
+    names = ORDER if args.workload == "all" else (args.workload,)
+    head = HEADLINE if args.workload == "all" else args.workload
+    peaks = load_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    out = {}
+    try:
+        for name in names:
+            _, groups = workloads.expert_parallel_groups(name, ws, rank)
+            rec = measure_workload(name, groups, args, dev, ws, sampler)
+            s = summary_of(rec, args, ws, peaks)
+            if name == head:
+                s["e2e"] = measure_e2e(rec, args, dev, ws)
+            if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+                cpu, parity = oracle_check(rec, args.cpu_budget_s if name == head else args.cpu_check_s)
+                s["parity"] = parity
+                if name == head:
+                    s["cpu_baseline"] = dict(cpu, parity=parity)
+            del rec
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            out[name] = s
+    finally:
+        sampler.stop()
+    if rank == 0:
+        h = out[head]
+        line = {
+            "metric": METRIC, "value": h["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+            "data": "synthetic (seeded uniform / Gaussian-quantised FP4 codes and E4M3 scales)",
+            "config": h["config"],
+            "launch": ("one nvfp4_relayout_and_gemm call per step (relayout + grouped GEMM "
+                       "launches), K steps captured in one CUDA graph"),
+        }
+        for k in ("us_per_call", "isolated_us", "roofline", "relayout", "e2e", "gpu_launches", "clocks",
+                  "sustained", "cpu_baseline", "parity"):
+            if k in h:
+                line[k] = h[k]
+        if len(out) > 1:
+            line["per_config"] = {k: v for k, v in out.items() if k != head}
+        print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-
-
 def run_profile(args):
     """Minimal launch sequence for an ncu capture: `warmup` steps (flush,
     relayout, GEMM), then one more step; no timing, no oracle."""
@@ -657,10 +826,15 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="moe_gate_up")
+    ap.add_argument("--workload", default="all",
+                    help="all (default: every workload, the largest as the headline) or one name")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
+    ap.add_argument("--cpu-check-s", type=float, default=4.0,
+                    help="oracle seconds for the parity sample of each non-headline workload")
+    ap.add_argument("--sustain-s", type=float, default=1.0,
+                    help="length of each workload's sustained replay window (clock evidence)")
     ap.add_argument("--profile", action="store_true",
                     help="few launches for ncu: W warm-up steps, then one step")
     ap.add_argument("--op", default="gemm", choices=["gemm", "quantize"],
@@ -669,6 +843,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "all" and (args.profile or args.op == "quantize"):
+        args.workload = HEADLINE if args.profile else "moe_gate_up"
     if args.op == "quantize":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": "quantize",

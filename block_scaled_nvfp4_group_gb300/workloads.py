@@ -200,3 +200,42 @@ def describe(name: str) -> dict:
     else:
         shapes = [(4096, 4096, 4096)] * 4
     return {"name": name, "seed": seed, "shapes": shapes}
+
+
+# --- expert-parallel batches (one process per GPU) --------------------------
+
+def expert_parallel_shapes(name: str, world_size: int):
+    """Shapes of the global grouped call that `world_size` ranks share: the
+    workload's group list repeated `world_size` times (copy c holds the
+    experts of rank c's worth of work), so each rank keeps about one
+    workload's FLOPs (weak scaling)."""
+    if world_size < 1:
+        raise ValueError("world_size must be >= 1")
+    return list(describe(name)["shapes"]) * world_size
+
+
+def expert_parallel_groups(name: str, world_size: int, rank: int):
+    """The groups of the global grouped call (expert_parallel_shapes) that
+    `rank` owns, as (global indices, groups).  The split is
+    shard.shard_groups (longest processing time first by FLOPs); copy 0 of
+    the group list holds the workload's own data, copy c >= 1 draws group i
+    from its own seed, so every rank can build exactly its groups.  With
+    world_size 1 this is the workload itself."""
+    from . import shard
+    base = describe(name)
+    n = len(base["shapes"])
+    shapes = expert_parallel_shapes(name, world_size)
+    mine = shard.shard_groups(shapes, world_size, rank)
+    kind = "gaussian" if name == "quantized" else "uniform"
+    own = None
+    out = []
+    for gi in mine:
+        c, i = divmod(gi, n)
+        if c == 0:
+            if own is None:
+                own = make_workload(name).groups
+            out.append(own[i])
+        else:
+            seed = base["seed"] + 7919 + 1000 * c + i
+            out.append(make_groups([shapes[gi]], seed, kind)[0])
+    return mine, out

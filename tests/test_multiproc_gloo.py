@@ -77,3 +77,50 @@ def test_shard_balance_and_edges():
         shard.shard_groups(shapes, 2, 2)
     assert shard.rank_seed(1001, 0) == 1001 and shard.rank_seed(1001, 3) == 4001
     assert shard.max_over_ranks(2.5) == 2.5
+
+
+def _ep_worker(rank, world, port, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from block_scaled_nvfp4_group_gb300 import workloads
+        from oracle import oracle
+        idx, groups = workloads.expert_parallel_groups("tiny", world, rank)
+        res = {f"c{gi}": oracle.get().gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, threads=1)
+               for gi, g in zip(idx, groups)}
+        flops = sum(2 * g.M * g.N * g.K for g in groups)
+        np.savez(os.path.join(out_dir, f"ep{rank}.npz"), idx=np.array(idx), flops=flops, **res)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_expert_parallel_split(tmp_path):
+    """The split bench.py uses under torchrun: two ranks share one grouped
+    call of two copies of the workload's groups; every group is computed by
+    exactly one rank, each rank holds the same FLOPs, copy 0 is the workload
+    itself and copy 1 has its own data."""
+    port = _free_port()
+    mp.spawn(_ep_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    from block_scaled_nvfp4_group_gb300 import workloads
+    from oracle import oracle
+    shapes = workloads.expert_parallel_shapes("tiny", 2)
+    assert shapes == [(64, 256, 256), (128, 256, 256)] * 2
+    base = workloads.make_workload("tiny").groups
+    seen, flops, outs = [], [], {}
+    for r in range(2):
+        d = np.load(tmp_path / f"ep{r}.npz")
+        seen += d["idx"].tolist()
+        flops.append(int(d["flops"]))
+        for gi in d["idx"].tolist():
+            outs[gi] = d[f"c{gi}"]
+    assert sorted(seen) == [0, 1, 2, 3]
+    assert flops[0] == flops[1]
+    for i, g in enumerate(base):
+        ref = oracle.get().gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K, threads=1)
+        assert np.array_equal(outs[i], ref)
+    # copy 1 draws its own inputs: same shapes, different C
+    assert outs[2].shape == outs[0].shape and not np.array_equal(outs[2], outs[0])
+    # one rank alone gets the workload itself
+    idx1, g1 = workloads.expert_parallel_groups("tiny", 1, 0)
+    assert idx1 == [0, 1] and all(np.array_equal(a.A, b.A) for a, b in zip(g1, base))
