@@ -22,8 +22,9 @@ NVFP4_ERR_TOO_MANY = -6
 
 # kernel configurations (NVFP4_KIND_* in the header) and their kernels
 KIND_NAMES = {0: "stream", 1: "wide", 2: "compute", 3: "wide512", 4: "wide_p2", 5: "wide_p4",
-              6: "pair", 7: "wide_sk"}
-KIND_KERNELS = {k: ("nvfp4_group_gemm_pair_kernel" if k == 6 else "nvfp4_group_gemm_kernel")
+              6: "pair", 7: "wide_sk", 8: "swap"}
+KIND_KERNELS = {k: ("nvfp4_group_gemm_pair_kernel" if k == 6 else
+                    "nvfp4_group_gemm_swap_kernel" if k == 8 else "nvfp4_group_gemm_kernel")
                 for k in KIND_NAMES}
 
 

@@ -9,7 +9,7 @@
 #include <vector>
 
 #include "../../include/nvfp4_group_gemm.h"
-#include "gemm_pair_kernel.cuh"
+#include "gemm_swap_kernel.cuh"
 #include "runtime.h"
 
 namespace nvfp4 {
@@ -30,7 +30,8 @@ enum Kind : int {
     kKindWideP4 = NVFP4_KIND_WIDE_P4,
     kKindPair = NVFP4_KIND_PAIR,
     kKindWideSK = NVFP4_KIND_WIDE_SK,
-    kNumKinds = 8
+    kKindSwap = NVFP4_KIND_SWAP,
+    kNumKinds = 9
 };
 
 bool needs_n256(int kind)
@@ -128,12 +129,23 @@ KindInfo make_pair_kind()
                     &launch_pair_kind<Cfg>};
 }
 
+// the swapped-operand pair kernel takes its own parameter block
+// (plan_and_launch_swap); its entry here serves the attributes and the
+// cluster occupancy query only
+KindInfo make_swap_kind()
+{
+    return KindInfo{CfgSwap::BW, kSwapMaxTok, kBM, 1, CfgSwap::kMmas, 1, 32, CfgSwap::kThreads,
+                    CfgSwap::kSmemBytes, true, false,
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_swap_kernel<CfgSwap, false>),
+                    reinterpret_cast<const void *>(&nvfp4_group_gemm_swap_kernel<CfgSwap, true>), nullptr};
+}
+
 const KindInfo &kind_info(int k)
 {
     static const KindInfo table[kNumKinds] = {
         make_kind<CfgStream>(),  make_kind<CfgWide>(), make_kind<CfgCompute>(),
         make_kind<CfgWide512>(), make_kind<CfgWide>(), make_kind<CfgWide>(),
-        make_pair_kind<CfgPair>(), make_kind<CfgWide, true>()};
+        make_pair_kind<CfgPair>(), make_kind<CfgWide, true>(), make_swap_kind()};
     return table[canonical_kind(k)];
 }
 
@@ -229,7 +241,7 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
     const int forced_env = env_int("NVFP4_GEMM_KIND", -1);
     // SwiGLU pairs the two 128-column halves of a 256-column tile
     const int forced = (need_bn256 && forced_env >= 0 && forced_env < kNumKinds &&
-                        kind_info(forced_env).bn != 256)
+                        (kind_info(forced_env).bn != 256 || forced_env == kKindSwap))
                            ? kKindWide
                            : forced_env;
     bool all_n256 = true, all_n_ge256 = true;
@@ -411,6 +423,183 @@ int plan_and_launch(const GroupDesc *groups, int num_groups, cudaStream_t stream
     return rc;
 }
 
+// ---------------------------------------------------------------------------
+// SWAP: the transposed product on CTA pairs (gemm_swap_kernel.cuh)
+// ---------------------------------------------------------------------------
+
+// Token tiles of a group of M rows: at most 256 rows each, starting at
+// multiples of 128 rows (where the tiled scales start a new 128-row block);
+// a remainder of 257..384 rows is split 128 + rest, so both tiles stay
+// within 256 rows and as even as the 128-row grid allows.  Returns the tile
+// count and writes the start rows (and, past the last, M) to starts.
+int token_tiles(int M, int *starts, int cap)
+{
+    int n = 0, m = 0;
+    while (m < M && n < cap) {
+        const int rem = M - m;
+        const int take = rem <= kSwapMaxTok ? rem : (rem <= kSwapMaxTok + 128 ? 128 : kSwapMaxTok);
+        starts[n++] = m;
+        m += take;
+    }
+    starts[n] = m;
+    return m == M ? n : -1;
+}
+
+// number of token tiles token_tiles() makes for a group of M > 0 rows
+int token_tile_count(int M)
+{
+    int n = 0, rem = M;
+    while (rem > kSwapMaxTok + 128) {
+        ++n;
+        rem -= kSwapMaxTok;
+    }
+    return n + (rem > kSwapMaxTok ? 2 : 1);
+}
+
+// launches of a swap call: a new launch when either the group or the token
+// tile table of the current one is full (a group's token tiles may continue
+// in the next launch); must agree with plan_and_launch_swap
+int count_launches_swap(const GroupDesc *groups, int num_groups)
+{
+    int launches = 0, nw = 0, nt = 0;
+    for (int i = 0; i < num_groups; ++i) {
+        const GroupDesc &g = groups[i];
+        if (g.M == 0)
+            continue;
+        int left = token_tile_count(g.M);
+        while (left > 0) {
+            if (launches == 0 || nw == kSwapMaxW || nt == kSwapMaxT) {
+                ++launches;
+                nw = 0;
+                nt = 0;
+            }
+            const int take = left < kSwapMaxT - nt ? left : kSwapMaxT - nt;
+            ++nw;
+            nt += take;
+            left -= take;
+        }
+    }
+    return launches;
+}
+
+// Plan and launch a validated call on the swap kernel: every group's token
+// tiles, their tensor maps (offset pointers into A, the tiled SFA and C),
+// the group's B maps, one parameter block per launch.  All maps are encoded
+// before the first launch.
+template <class ErrFn>
+int plan_and_launch_swap(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev,
+                         ErrFn err_for_launch, const GemmEpilogue *epi, bool early_ab)
+{
+    const bool out_bf16 = epi && epi->out_bf16;
+    bool any_alpha = false;
+    if (epi && epi->alpha)
+        for (int i = 0; i < num_groups; ++i)
+            any_alpha = any_alpha || epi->alpha[i] != 1.0f;
+    const bool ex = out_bf16 || any_alpha;
+    static thread_local std::vector<SwapParams> plist;
+    static thread_local std::vector<int> starts;
+    const CUtensorMapDataType c_type =
+        out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    plist.clear();
+    int rc = NVFP4_OK;
+    for (int i = 0; i < num_groups && rc == NVFP4_OK; ++i) {
+        const GroupDesc &g = groups[i];
+        if (g.M == 0)
+            continue;
+        starts.resize((size_t)token_tile_count(g.M) + 1);
+        const int ntt = token_tiles(g.M, starts.data(), (int)starts.size() - 1);
+        if (ntt != token_tile_count(g.M))
+            return NVFP4_ERR_INVALID_ARGUMENT;
+        const int wt = (g.N + CfgSwap::BW - 1) / CfgSwap::BW;
+        int done = 0;
+        while (done < ntt && rc == NVFP4_OK) {
+            if (plist.empty() || plist.back().num_w == kSwapMaxW ||
+                plist.back().num_w == 0 ||
+                plist.back().w_tfirst[plist.back().num_w - 1] + plist.back().w_tcount[plist.back().num_w - 1] ==
+                    kSwapMaxT) {
+                plist.emplace_back();
+                std::memset(&plist.back(), 0, sizeof(SwapParams));
+                SwapParams &P = plist.back();
+                P.err = err_for_launch((int)plist.size() - 1);
+                P.timeout_ns = wait_timeout_ns();
+                P.b_policy = choose_b_policy();
+                P.pf_stages = choose_prefetch();
+                P.debug_drop_stage = debug_drop_stage();
+                P.out_bf16 = out_bf16 ? 1 : 0;
+                P.early_ab = early_ab ? 1 : 0;
+            }
+            SwapParams &P = plist.back();
+            const int w = P.num_w;
+            const int t0 = w > 0 ? P.w_tfirst[w - 1] + P.w_tcount[w - 1] : 0;
+            const int take = (ntt - done) < (kSwapMaxT - t0) ? (ntt - done) : (kSwapMaxT - t0);
+            rc = encode_map_operand(&P.tmW[w], g.B, (uint64_t)g.N, (uint64_t)g.K, kBM, 1);
+            if (rc == NVFP4_OK)
+                rc = encode_map_sf(&P.tmSW[w], g.SFB, (uint64_t)g.N, (uint64_t)g.K, CfgSwap::kMmas, 1);
+            for (int k = 0; k < take && rc == NVFP4_OK; ++k) {
+                const int t = t0 + k;
+                const int m0 = starts[done + k], mt = starts[done + k + 1] - m0;
+                const int npad = (mt + 15) / 16 * 16;
+                const int nsx = (mt + 127) / 128;
+                const uint8_t *a = static_cast<const uint8_t *>(g.A) + (size_t)m0 * (size_t)(g.K / 2);
+                const uint8_t *sa =
+                    static_cast<const uint8_t *>(g.SFA) + (size_t)(m0 / 128) * (size_t)(g.K / 64) * 512u;
+                uint8_t *c = static_cast<uint8_t *>(g.C) + (size_t)m0 * (size_t)g.N * 2u;
+                rc = encode_map_operand(&P.tmX[t], a, (uint64_t)mt, (uint64_t)g.K, (uint32_t)(npad / 2), 1);
+                if (rc == NVFP4_OK)
+                    rc = encode_map_sf(&P.tmSX[t], sa, (uint64_t)mt, (uint64_t)g.K, CfgSwap::kMmas, (uint32_t)nsx);
+                if (rc == NVFP4_OK)
+                    rc = encode_map_2d(&P.tmC[t], c_type, c, (uint64_t)g.N, (uint64_t)mt, (uint64_t)g.N * 2, 32, 32,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                P.t_group[t] = w;
+                P.t_rows[t] = mt;
+                P.t_npad[t] = npad;
+                P.t_sfx[t] = nsx;
+            }
+            P.w_N[w] = g.N;
+            P.w_kchunks[w] = g.K / kChunkK;
+            P.w_tiles[w] = wt;
+            P.w_tfirst[w] = t0;
+            P.w_tcount[w] = take;
+            P.alpha[w] = (epi && epi->alpha) ? epi->alpha[i] : 1.0f;
+            P.total_tiles += wt * take;
+            P.tile_end[w] = P.total_tiles;
+            P.num_w = w + 1;
+            done += take;
+        }
+    }
+    for (size_t l = 0; l < plist.size() && rc == NVFP4_OK; ++l) {
+        const SwapParams &P = plist[l];
+        const int pairs = g_max_pairs[dev][kKindSwap];
+        const int grid = 2 * (P.total_tiles < pairs ? P.total_tiles : pairs);
+        LaunchCfg L;
+        make_launch_cfg(L, grid, CfgSwap::kThreads, CfgSwap::kSmemBytes, true, stream);
+        const cudaError_t e = ex ? cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_swap_kernel<CfgSwap, true>, P)
+                                 : cudaLaunchKernelEx(&L.cfg, nvfp4_group_gemm_swap_kernel<CfgSwap, false>, P);
+        if (e != cudaSuccess || cudaGetLastError() != cudaSuccess)
+            rc = NVFP4_ERR_CUDA;
+    }
+    return rc;
+}
+
+// launches of a call on `kind` (0: every group empty)
+int launches_of(const GroupDesc *groups, int num_groups, int kind)
+{
+    if (kind == kKindSwap)
+        return count_launches_swap(groups, num_groups);
+    return count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn);
+}
+
+// the launches of a validated call on `kind`
+template <class ErrFn>
+int dispatch(const GroupDesc *groups, int num_groups, cudaStream_t stream, int dev, int sm_count, int kind,
+             ErrFn err_for_launch, const GemmEpilogue *epi = nullptr, const SkScratch *sk = nullptr,
+             bool early_ab = false)
+{
+    if (kind == kKindSwap)
+        return plan_and_launch_swap(groups, num_groups, stream, dev, err_for_launch, epi, early_ab);
+    return plan_and_launch(groups, num_groups, stream, dev, sm_count, kind, err_for_launch, epi, sk, early_ab);
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -425,7 +614,7 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
     if (rc != NVFP4_OK)
         return rc;
     int kind = choose_kind(groups, num_groups, dev->sm_count);
-    if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+    if (launches_of(groups, num_groups, kind) == 0)
         return NVFP4_OK;
     SkScratch sk{};
     if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
@@ -436,7 +625,7 @@ extern "C" int nvfp4_group_gemm(const GroupDesc *groups, int num_groups, cudaStr
     if (rc != NVFP4_OK)
         return rc;
     uint32_t *err = dev->err;
-    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
+    return dispatch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; }, nullptr, &sk);
 }
 
@@ -457,7 +646,7 @@ extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, cons
     if (rc != NVFP4_OK)
         return rc;
     int kind = choose_kind(groups, num_groups, dev->sm_count, swiglu);
-    if (count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+    if (launches_of(groups, num_groups, kind) == 0)
         return NVFP4_OK;
     SkScratch sk{};
     if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
@@ -468,7 +657,7 @@ extern "C" int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, cons
     if (rc != NVFP4_OK)
         return rc;
     uint32_t *err = dev->err;
-    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
+    return dispatch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; }, epi, &sk);
 }
 
@@ -517,7 +706,7 @@ extern "C" int nvfp4_relayout_and_gemm(const StepDesc *steps, int num_groups, co
     if (rc != NVFP4_OK)
         return rc;
     int kind = choose_kind(groups.data(), num_groups, dev->sm_count, swiglu);
-    if (count_launches(groups.data(), num_groups, kind_info(kind).bm, kind_info(kind).bn) == 0)
+    if (launches_of(groups.data(), num_groups, kind) == 0)
         return NVFP4_OK;
     SkScratch sk{};
     if (kind == kKindWideSK && sk_scratch(stream, dev->sm_count, &sk) != NVFP4_OK)
@@ -531,7 +720,7 @@ extern "C" int nvfp4_relayout_and_gemm(const StepDesc *steps, int num_groups, co
     if (rc != NVFP4_OK)
         return rc;
     uint32_t *err = dev->err;
-    return plan_and_launch(groups.data(), num_groups, stream, dev_id, dev->sm_count, kind,
+    return dispatch(groups.data(), num_groups, stream, dev_id, dev->sm_count, kind,
                            [err](int) { return err; }, epi, &sk, true);
 }
 
@@ -546,7 +735,7 @@ extern "C" int nvfp4_group_gemm_plan_for(const GroupDesc *groups, int num_groups
         return rc;
     const int k = choose_kind(groups, num_groups, sm_count);
     *kind = k;
-    *launches = count_launches(groups, num_groups, kind_info(k).bm, kind_info(k).bn);
+    *launches = launches_of(groups, num_groups, k);
     return NVFP4_OK;
 }
 
@@ -644,7 +833,7 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
     if (kind == kKindWideSK)
         kind = kKindWide;
     // each launch needs its own two status words of the static scratch
-    const int launches = count_launches(groups, num_groups, kind_info(kind).bm, kind_info(kind).bn);
+    const int launches = launches_of(groups, num_groups, kind);
     if (launches == 0)
         return NVFP4_OK;
     if (launches > kNoAllocMaxLaunches)
@@ -659,6 +848,6 @@ extern "C" int nvfp4_group_gemm_noalloc(const GroupDesc *groups, int num_groups,
     if (cudaMemsetAsync(dev->scratch, 0, sizeof(uint32_t) * 2 * launches, stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     uint32_t *scratch = dev->scratch;
-    return plan_and_launch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
+    return dispatch(groups, num_groups, stream, dev_id, dev->sm_count, kind,
                            [scratch](int l) { return scratch + 2 * l; });
 }

@@ -126,7 +126,18 @@ int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilo
  *          stream is being captured into a graph at that moment) the call
  *          runs as WIDE.  Sums of cut tiles are formed in a different order,
  *          so results may differ from WIDE in the last bits of FP32 before
- *          rounding. */
+ *          rounding.
+ *  SWAP    the transposed product C^T = B . A^T on CTA pairs: 256 rows of B
+ *          as the MMA's M side and a tile of <= 256 rows of A (a group's
+ *          tokens; larger groups are split into tiles 128 or 256 rows
+ *          apart) as its N side, rounded up to 16, so each B byte is staged
+ *          once per token tile and no MMA work goes to padding rows beyond
+ *          that rounding; the epilogue transposes through shared memory
+ *          before its stores.  Any N; no SwiGLU (a forced SWAP call with
+ *          SwiGLU runs as WIDE).  Only selected through NVFP4_GEMM_KIND=8:
+ *          on GB300 it measured slower than WIDE on the MoE shapes it was
+ *          built for (each stage's scale copies sit on the pair's critical
+ *          path). */
 enum {
     NVFP4_KIND_STREAM = 0,
     NVFP4_KIND_WIDE = 1,
@@ -135,7 +146,8 @@ enum {
     NVFP4_KIND_WIDE_P2 = 4,
     NVFP4_KIND_WIDE_P4 = 5,
     NVFP4_KIND_PAIR = 6,
-    NVFP4_KIND_WIDE_SK = 7
+    NVFP4_KIND_WIDE_SK = 7,
+    NVFP4_KIND_SWAP = 8
 };
 
 /* The plan nvfp4_group_gemm would follow for these groups on the current
@@ -162,8 +174,8 @@ int nvfp4_group_gemm_plan_for(const GroupDesc *groups, int num_groups, int sm_co
  * run, and latency-critical loops that cannot afford the device-wide
  * synchronisation an allocation may bring.  nvfp4_group_gemm allocates a
  * 16-byte status word on its first call on a device; this entry point
- * allocates nothing, ever.  (The pages have no counterpart: their launchers
- * cudaMalloc a parameter buffer.)
+ * allocates nothing, ever.  The pages have no counterpart of this entry
+ * point.
  *
  * Arguments, layouts, limits and results are those of nvfp4_group_gemm, with
  * one more limit: the kernel's status record (two 32-bit words per kernel

@@ -54,7 +54,7 @@ def compare_bf16(got_bits: np.ndarray, ref_bits: np.ndarray, what: str) -> None:
 
 
 KINDS = {"stream": 0, "wide": 1, "compute": 2, "wide512": 3, "wide_p2": 4, "wide_p4": 5,
-         "pair": 6, "wide_sk": 7}
+         "pair": 6, "wide_sk": 7, "swap": 8}
 
 
 class gemm_env:

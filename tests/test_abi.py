@@ -178,6 +178,11 @@ def test_plan_kind_and_launches(lib, monkeypatch, shapes, sm, kind, launches):
     ("0", [(m, 4096, 7168) for m in MOE_M], "stream"),
     ("7", [(m, 4096, 7168) for m in MOE_M], "wide_sk"),
     ("6", [(m, 4096, 7168) for m in MOE_M], "pair"),
+    ("1", [(m, 4096, 7168) for m in MOE_M], "wide"),
+    ("8", [(4096, 4096, 256)], "swap"),
+    ("8", [(m, 4096, 7168) for m in MOE_M], "swap"),
+    # the swapped kernel takes any N (rows of B past N load as zeros)
+    ("8", [(77, 136, 512)], "swap"),
     ("1", [(4096, 4096, 4096)] * 4, "wide"),
     # a forced kind that cannot take the shapes falls back to 128-column tiles
     ("1", [(77, 136, 512)], "stream"),
@@ -191,6 +196,21 @@ def test_plan_forced_kind(lib, monkeypatch, forced, shapes, kind):
     rc, k, n = _plan(lib, shapes)
     assert (rc, k) == (_abi.NVFP4_OK, kind)
     assert n == 1
+
+
+def test_plan_swap_token_tiles_across_launches(lib, monkeypatch):
+    # 4096 rows = 16 token tiles per group: 4 groups fill two launches of 32
+    # token tiles; a group's tiles may continue in the next launch; a swap
+    # launch takes 16 groups and 32 token tiles, empty groups take no slot
+    monkeypatch.setenv("NVFP4_GEMM_KIND", "8")
+    assert _plan(lib, [(64, 256, 256)] * 16) == (_abi.NVFP4_OK, "swap", 1)
+    assert _plan(lib, [(64, 256, 256)] * 17) == (_abi.NVFP4_OK, "swap", 2)
+    assert _plan(lib, [(300, 256, 256)] * 17) == (_abi.NVFP4_OK, "swap", 2)
+    assert _plan(lib, [(0, 256, 256)] * 40 + [(64, 256, 256)] * 30) == (_abi.NVFP4_OK, "swap", 2)
+    assert _plan(lib, [(384, 4096, 256)] * 16) == (_abi.NVFP4_OK, "swap", 1)
+    assert _plan(lib, [(4096, 4096, 4096)] * 4) == (_abi.NVFP4_OK, "swap", 2)
+    assert _plan(lib, [(4096, 4096, 4096)] * 4 + [(1, 256, 256)]) == (_abi.NVFP4_OK, "swap", 3)
+    assert _plan(lib, [(2 << 18, 256, 256)]) == (_abi.NVFP4_OK, "swap", 64)
 
 
 def test_plan_pair_launch_counts_256_row_tiles(lib, monkeypatch):

@@ -50,14 +50,14 @@ def _check(groups, alpha, out_bf16, swiglu, kind=None):
 SHAPES = [(200, 512, 1024), (77, 256, 512), (300, 768, 256), (1, 256, 2304)]
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide", "pair"])
+@pytest.mark.parametrize("kind", [None, "stream", "wide", "pair", "swap"])
 def test_alpha_fp16(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     groups = workloads.make_groups(SHAPES, seed=51)
     _check(groups, [0.5, 0.0078125, 3.0, -1.25], False, False, kind)
 
 
-@pytest.mark.parametrize("kind", [None, "pair"])
+@pytest.mark.parametrize("kind", [None, "pair", "swap"])
 def test_bf16_output(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     groups = workloads.make_groups(SHAPES, seed=52)
@@ -65,12 +65,13 @@ def test_bf16_output(kind):
     _check(groups, [0.1, 0.2, 0.3, 0.4], True, False, kind)
 
 
-@pytest.mark.parametrize("kind", [None, "wide", "pair", "stream"])
+@pytest.mark.parametrize("kind", [None, "wide", "pair", "stream", "swap"])
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_swiglu(kind, out_bf16):
     """SwiGLU with small per-group scales (the gate/up sums of these inputs
     reach the hundreds; the products would overflow FP16 unscaled).  A
-    forced 128-wide configuration falls back to the 256-wide one."""
+    forced 128-wide or swapped configuration falls back to the 256-wide
+    one."""
     from block_scaled_nvfp4_group_gb300 import workloads
     groups = workloads.make_groups(SHAPES, seed=53)
     _check(groups, [1 / 64, 1 / 32, 1 / 128, 1 / 16], out_bf16, True, kind)

@@ -11,7 +11,7 @@ from oracle import oracle
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kind", [None, "pair", "wide_sk"])
+@pytest.mark.parametrize("kind", [None, "swap", "pair", "wide_sk"])
 def test_expired_wait_reports_timeout_and_context_survives(kind):
     require_gb300()
     with gemm_env(kind):

@@ -93,12 +93,40 @@ def test_pair_tiles_ragged():
         run_and_compare(workloads.make_groups(shapes, seed=22))
 
 
-def test_more_groups_than_one_launch():
+@pytest.mark.parametrize("kind", [None, "swap"])
+def test_more_groups_than_one_launch(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     rng = np.random.default_rng(4)
     shapes = [(int(rng.integers(1, 200)), 8 * int(rng.integers(1, 40)), 256 * int(rng.integers(1, 4)))
               for _ in range(40)]
-    run_and_compare(workloads.make_groups(shapes, seed=4))
+    with gemm_env(kind):
+        run_and_compare(workloads.make_groups(shapes, seed=4))
+
+
+@pytest.mark.parametrize("pf", [None, 0, 2])
+def test_swap_token_tiles_ragged(pf):
+    """The transposed product on CTA pairs: token tiles of every size class
+    (1, 5, 45 rows: MMA N = 16..48; 129: two token scale blocks; 256 and
+    257: one full tile and a split into 128 + 129; 385, 513: tiles of 256
+    and a remainder), N past the 256 grid (264, 520: the odd CTA's rows of B
+    partly or wholly past N), N below 256, one- and multi-stage K, an empty
+    group, more tiles than pairs; with the L2 prefetch of B off and on."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(1, 256, 256), (5, 512, 768), (45, 256, 2304), (77, 264, 512), (0, 256, 256),
+              (129, 768, 256), (200, 256, 1024), (256, 512, 512), (257, 256, 256), (300, 520, 768),
+              (385, 256, 512), (513, 256, 256), (64, 136, 256), (7, 8, 256)]
+    with gemm_env("swap", pf):
+        run_and_compare(workloads.make_groups(shapes, seed=23))
+
+
+def test_swap_many_token_tiles_and_launches():
+    """A forced swapped call whose groups need more token tiles than one
+    launch holds (1100 rows = 5 token tiles each; 20 groups), so groups
+    continue across launches, with K wrapping the ring several times."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    shapes = [(1100, 256, 1536)] * 7 + [(97, 512, 256)] * 13
+    with gemm_env("swap"):
+        run_and_compare(workloads.make_groups(shapes, seed=24), rows_per_group=40, seed=5)
 
 
 def test_full_scale_range_and_signs():
@@ -162,21 +190,21 @@ def test_workload_tiny():
     run_and_compare(workloads.make_workload("tiny").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "wide", "pair"])
+@pytest.mark.parametrize("kind", [None, "wide", "pair", "swap"])
 def test_workload_quantized(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
         run_and_compare(workloads.make_workload("quantized").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute", "pair"])
+@pytest.mark.parametrize("kind", [None, "swap", "stream", "wide512", "compute", "pair"])
 def test_workload_moe_down(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
         run_and_compare(workloads.make_workload("moe_down").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "stream", "wide512", "compute", "pair"])
+@pytest.mark.parametrize("kind", [None, "swap", "stream", "wide512", "compute", "pair"])
 def test_workload_moe_gate_up(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
@@ -190,7 +218,7 @@ def test_workload_square_sampled_rows(kind):
         run_and_compare(workloads.make_workload("square").groups, rows_per_group=24, seed=9)
 
 
-@pytest.mark.parametrize("kind", [None, "pair"])
+@pytest.mark.parametrize("kind", [None, "pair", "swap"])
 def test_step_graph_replays_new_inputs(kind):
     """The step as bench.py times it: one nvfp4_relayout_and_gemm call (scale
     relayout + grouped GEMM) captured as a CUDA graph on a side stream and
@@ -227,7 +255,7 @@ def test_step_graph_replays_new_inputs(kind):
             compare_fp16(c, o.gemm(gr.A, gr.SFA, gr.B, gr.SFB, gr.M, gr.N, gr.K), f"replay {rep}")
 
 
-def test_plan_picks_pairs_only_for_large_m():
+def test_plan_picks_by_shape_class():
     """The configuration the library picks per shape class: CTA pairs for
     the 4096^3 groups, 128 x 256 tiles for the small-M MoE shapes, 128 x 128
     tiles when some N is not a multiple of 256; one launch per 32 groups."""
