@@ -87,3 +87,60 @@ def test_noalloc_refuses_more_than_its_scratch_holds():
     arr = (_abi.GroupDesc * n)(*[_abi.GroupDesc(256, 256, 256, 256, 256, 1, 8, 256)
                                  for _ in range(n)])
     assert lib.nvfp4_group_gemm_noalloc(arr, n, None) == _abi.NVFP4_ERR_TOO_MANY
+
+
+_FIRST_CALL_SCRIPT = r"""
+import ctypes, sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+from block_scaled_nvfp4_group_gb300 import _abi, workloads
+from oracle import oracle
+lib = _abi.load()
+o = oracle.get()
+torch.cuda.init()
+shapes = [(130, 264, 512), (64, 256, 256)]
+groups = workloads.make_groups(shapes, seed=33)
+keep, descs = [], (_abi.GroupDesc * len(groups))()
+for i, g in enumerate(groups):
+    # tiled scales made on the host, so that no other library call precedes
+    sa = torch.from_numpy(o.sf_relayout(g.SFA, g.M, g.K)).cuda()
+    sb = torch.from_numpy(o.sf_relayout(g.SFB, g.N, g.K)).cuda()
+    A = torch.from_numpy(g.A).cuda().reshape(-1)
+    B = torch.from_numpy(g.B).cuda().reshape(-1)
+    C = torch.full((g.M, g.N), float("nan"), dtype=torch.float16, device="cuda")
+    keep.append((A, B, sa, sb, C))
+    descs[i] = _abi.GroupDesc(A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(),
+                              g.M, g.N, g.K)
+torch.cuda.synchronize()
+stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+free = []
+for call in range(2):
+    rc = lib.nvfp4_group_gemm_noalloc(descs, len(groups), stream)
+    assert rc == _abi.NVFP4_OK, rc
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+print("FREE", free[0], free[1])
+for g, (_, _, _, _, C) in zip(groups, keep):
+    ref = o.gemm(g.A, g.SFA, g.B, g.SFB, g.M, g.N, g.K).view(np.float16).astype(np.float64)
+    got = C.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-3 * np.abs(ref) + 1e-2), "mismatch"
+print("FIRST_CALL_OK")
+"""
+
+
+def test_noalloc_as_first_library_call_in_a_fresh_process():
+    """In a process whose first library call is the no-allocation entry
+    point (tiled scales prepared on the host), the output equals the
+    oracle's, and a second call leaves the device's free memory unchanged."""
+    require_gb300()
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_SCRIPT, root], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    assert "FIRST_CALL_OK" in r.stdout
+    free = [int(x) for x in next(ln for ln in r.stdout.splitlines() if ln.startswith("FREE")).split()[1:]]
+    assert free[0] == free[1], free
