@@ -18,9 +18,11 @@
 // atoms; narrower tiles than a whole row leave a smaller last round of CTAs).
 // Warp w walks rows 32 w .. 32 w + 31, four rows per step: lane i takes the
 // 16-element block i % 8 of row 4 s + i / 8 (two 16-byte loads; a warp reads
-// four 256-byte row pieces), four steps in flight, so every block's absmax,
-// scale and codes stay in one lane; its sixteen codes go out as one 8-byte
-// store.  Scales are staged in shared memory in the tiled atom layout (and
+// four 256-byte row pieces), four steps in flight -- or all eight, so the
+// CTA makes a single round trip to memory, when the whole grid is resident
+// at once (one wave: latency, not bandwidth, is then what bounds it) -- so
+// every block's absmax, scale and codes stay in one lane; its sixteen codes
+// go out as one 8-byte store.  Scales are staged in shared memory in the tiled atom layout (and
 // row-major) and leave in 16-byte stores at the end.
 // The quotients absmax / 6 and x / scale are formed as q = a r with r = 1 /
 // divisor correctly rounded (a constant, or a 128-entry shared-memory table
@@ -53,7 +55,6 @@ constexpr int kCols = 128;       // K elements per CTA (two scale atoms)
 constexpr int kThreads = 128;
 constexpr int kLanesPerRow = kCols / 16;   // one lane per 16-element block
 constexpr int kRowsPerStep = 32 / kLanesPerRow;
-constexpr int kUnroll = 4;       // steps in flight per warp
 static_assert(kThreads == 128, "one thread per E4M3 code fills the scale tables");
 
 __device__ __forceinline__ uint32_t e4m3_of(float s)
@@ -121,8 +122,9 @@ struct QuantParams {
     int rows, K;
 };
 
-template <bool BF16>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constant__ QuantParams p)
+// UNROLL: steps (of four rows per warp) in flight, 4 or 8
+template <bool BF16, int UNROLL>
+__global__ void __launch_bounds__(kThreads, UNROLL == 8 ? 6 : 8) quantize_kernel(const __grid_constant__ QuantParams p)
 {
     __shared__ __align__(16) uint8_t atoms[kCols / 64][512];   // the tile's scale atoms
     __shared__ __align__(16) uint8_t rm[kRows][kCols / 16];    // the same scales, row-major
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const __grid_constan
     const int sub = lane / kLanesPerRow;        // row of the step
     const int col = c0 + 16 * j;                // this lane's first column
     const bool in_k = col < p.K;                // K % 64 == 0: whole blocks
+    constexpr int kUnroll = UNROLL;
+    static_assert(32 % (kUnroll * kRowsPerStep) == 0, "steps must tile the warp's 32 rows");
     for (int rr = 0; rr < 32; rr += kUnroll * kRowsPerStep) {
         uint4 v[kUnroll][2];
 #pragma unroll
@@ -249,8 +253,17 @@ extern "C" int nvfp4_quantize(const void *x, int x_is_bf16, int rows, int K, voi
     attr[0].val.programmaticStreamSerializationAllowed = env_int("NVFP4_PDL", 1) != 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = x_is_bf16 ? cudaLaunchKernelEx(&cfg, quantize_kernel<true>, p)
-                                    : cudaLaunchKernelEx(&cfg, quantize_kernel<false>, p);
+    // a grid that is resident all at once (one wave at the occupancy of the
+    // eight-step form, 6 CTAs per SM) takes eight steps in flight
+    const long long ctas = (long long)cfg.gridDim.x * cfg.gridDim.y;
+    const bool one_wave = ctas <= 6ll * dev->sm_count;
+    cudaError_t e;
+    if (one_wave)
+        e = x_is_bf16 ? cudaLaunchKernelEx(&cfg, quantize_kernel<true, 8>, p)
+                      : cudaLaunchKernelEx(&cfg, quantize_kernel<false, 8>, p);
+    else
+        e = x_is_bf16 ? cudaLaunchKernelEx(&cfg, quantize_kernel<true, 4>, p)
+                      : cudaLaunchKernelEx(&cfg, quantize_kernel<false, 4>, p);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
