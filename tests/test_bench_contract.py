@@ -64,3 +64,45 @@ def test_oracle_sample_and_parity_count():
         v[0, 0] = np.float16(float(v[0, 0]) + 1.0 + 0.01 * abs(float(v[0, 0])))
         assert bench.fp16_mismatches(worse, ref) == 1
     assert bench.time_oracle(wl, 0.05)[4] is None
+
+
+def test_rotating_copies_exceed_twice_the_l2():
+    """Between two uses of one copy's inputs the other copies' inputs total
+    at least 2 x L2; workloads needing more than 64 copies flush instead."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for nbytes in (69 * 10**6, 140 * 10**6, 15 * 10**6, 300 * 10**6):
+        r = bench.copies_needed(nbytes)
+        assert r >= 2 and (r - 1) * nbytes >= 2 * bench.L2_BYTES
+        assert (r - 2) * nbytes < 2 * bench.L2_BYTES        # no more copies than needed
+    assert bench.copies_needed(200 * 10**3) == 0             # tiny: flush protocol
+
+
+def test_roofline_and_summary_arithmetic():
+    """The roofline picks the larger of the byte and FLOP times, divides the
+    algorithmic work per launch by the mean launch time, and the summary's
+    value is FLOPs per step time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from block_scaled_nvfp4_group_gb300 import workloads
+    peaks = {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0, "source": "test"}
+
+    def rec(name, shapes, gemm_ms, launches=1):
+        return {"name": name, "flops": bench.flops_of(shapes), "gemm_bytes": bench.bytes_of(shapes),
+                "gemm_ms": gemm_ms * launches, "launches_per_step": 1 + launches, "kernel": "k", "kind": "wide"}
+
+    moe = workloads.describe("moe_gate_up")["shapes"]
+    r = bench.roofline_of(rec("moe_gate_up", moe, 0.05), peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - bench.bytes_of(moe) / 50e-6 / 1e9) < 1e-6 * r["achieved"]
+    assert abs(r["frac"] - r["achieved"] / 8000.0) < 1e-12
+    sq = workloads.describe("square")["shapes"]
+    r = bench.roofline_of(rec("square", sq, 0.1), peaks)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0 * 6
+    assert abs(r["achieved"] - bench.flops_of(sq) / 100e-6 / 1e12) < 1e-6 * r["achieved"]
+    # two GEMM launches per call: the per-launch time halves the call's
+    r2 = bench.roofline_of(rec("square", sq, 0.1, launches=2), peaks)
+    assert abs(r2["launch_us"] - 100.0) < 1e-9
+    # traffic only while the recorded counters describe these sources
+    assert (r["traffic"] is not None) == (bench.NCU_TRAFFIC["square"]["kernel_sha"] == bench.kernel_source_hash())
+    assert bench.bytes_of([(0, 256, 256)]) == 0
