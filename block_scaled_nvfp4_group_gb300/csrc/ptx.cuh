@@ -35,16 +35,27 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Longest time one try_wait may keep the waiting thread suspended (ns).  The
+// thread resumes as soon as the phase completes; the hint only replaces the
+// system's much shorter default limit, so a waiting role thread goes round
+// its loop (abort flag, clock, try again) a few times per phase instead of
+// continuously and leaves issue slots and shared-memory bandwidth to the
+// working warps: measured 4 % on the compute-bound 4096^3 grouped call and
+// 3 % on a single-round call, the other workloads unchanged or faster.
+// Bounded waits check their deadline after every return, so a deadline is
+// noticed at most this much later.
+constexpr uint32_t kWaitSuspendNs = 10000;
+
 // true once the phase with parity `parity` has completed
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
