@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                ptx::mbar_arrive_cluster(acce_leader);
+                ptx::mbar_arrive_cluster_relaxed(acce_leader);   // publishes no memory
             const bool sw = EPI_EX && p.swiglu;
             const int on0 = sw ? n0 / 2 : n0;     // output columns
             const int oN = sw ? N / 2 : N;

@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                ptx::mbar_arrive_cluster(acce_leader);
+                ptx::mbar_arrive_cluster_relaxed(acce_leader);   // publishes no memory
             // 3. 32 x 32 blocks (32 tokens x this warp's 32 columns of C),
             // transposed into shared memory (row = token, 64 bytes), each
             // stored with one TMA tensor store; two staging buffers per warp
