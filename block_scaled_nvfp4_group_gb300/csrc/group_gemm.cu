@@ -289,12 +289,16 @@ int choose_b_policy()
     return (o >= 0 && o <= 2) ? o : 0;
 }
 
-// L2 prefetch distance for B, in stages ahead of the MMAs: 6 measured best
-// on the MoE shapes (the ring holds 4 stages); 0 turns the prefetcher off
+// L2 prefetch distance for B, in stages ahead of the MMAs; 0 (the default)
+// leaves the prefetch warp idle.  Since the barrier waits sleep instead of
+// polling, the loaders alone keep enough HBM reads in flight: measured with
+// the prefetcher off / 2 / 6 / 10 stages ahead, moe_gate_up 38.3-38.6 /
+// 39.3 / 41.2-41.4 / 41.9 us, moe_down 27.3-27.5 / 27.8 / 27.7-28.0 / 28.5,
+// square and single-round calls unchanged.
 int choose_prefetch()
 {
     const int forced = env_int("NVFP4_PF_STAGES", -1);
-    return forced >= 0 ? forced : 6;
+    return forced >= 0 ? forced : 0;
 }
 
 // launches a call needs for tile width bn (one per 32 non-empty groups,
