@@ -280,13 +280,18 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
     return all_n256 ? kKindWide : kKindStream;
 }
 
-// L2 policy for B and its scales: B is streamed once per M-tile of its
-// group, and the M-tiles of one B strip run side by side, so the default
-// keeps B at normal priority (A and the A scales are kept: evict_last)
+// L2 policy for B and its scales (0 normal, 1 evict_first, 2 evict_last;
+// A and the A scales are always evict_last).  B is read once per M-tile of
+// its group, by CTAs running side by side; keeping it (2) measured best in
+// the bench's back-to-back steps: GEMM / step us, evict_last against
+// normal, square 119.4-119.8 / 125.3 against 120.4 / 125.4, moe_gate_up
+// 38.1-38.2 / 46.3-46.4 against 38.4 / 46.9, moe_down 27.2 / 32.6 against
+// 27.2 / 33.0; evict_first was slower on every shape but the single-round
+// one (square 123.3, moe_down 28.5 us).
 int choose_b_policy()
 {
     const int o = b_policy_override();
-    return (o >= 0 && o <= 2) ? o : 0;
+    return (o >= 0 && o <= 2) ? o : 2;
 }
 
 // L2 prefetch distance for B, in stages ahead of the MMAs; 0 (the default)
