@@ -97,6 +97,18 @@ __device__ __forceinline__ uint32_t clear_negative_zeros(uint32_t w)
     return mag | (w & nonzero);
 }
 
+// 16-byte read-only load that skips L1 (every byte is read once) and asks
+// L2 for the whole 256-byte segment: 0.629 -> 0.639 of HBM on the MoE
+// activations [2004, 7168], 0.875 -> 0.894 on [16384, 4096]
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 template <bool BF16>
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
 {
@@ -157,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, UNROLL == 8 ? 6 : 8) quantize_kernel
             v[u][1] = make_uint4(0, 0, 0, 0);
             if (in_k && row < p.rows) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)row * p.K + col);
-                v[u][0] = __ldg(src);
-                v[u][1] = __ldg(src + 1);
+                v[u][0] = ld_stream_v4(src);
+                v[u][1] = ld_stream_v4(src + 1);
             }
         }
 #pragma unroll
