@@ -47,6 +47,13 @@ struct RelayoutParams {
     int total_units;
 };
 
+__device__ __forceinline__ void st_na_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_constant__ RelayoutParams p)
 {
     // programmatic launch: read and write global memory only once the
@@ -80,10 +87,13 @@ __global__ void __launch_bounds__(kThreads) sf_relayout_kernel(const __grid_cons
         v[q] = r < nrows ? __ldg(reinterpret_cast<const uint4 *>(src + (size_t)r * kcols)) : make_uint4(0, 0, 0, 0);
     }
     uint8_t *o = p.dst[d] + ((size_t)rb * (kcols / 4) + (size_t)(4 * cblk)) * 512 + l * 16;
-    *reinterpret_cast<uint4 *>(o) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-    *reinterpret_cast<uint4 *>(o + 512) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-    *reinterpret_cast<uint4 *>(o + 1024) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-    *reinterpret_cast<uint4 *>(o + 1536) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+    // stores that do not allocate in L1 (every byte is written once):
+    // relayout 6.77 -> 6.58 us on the MoE gate/up scales, 6.03 -> 5.89 us on
+    // the 4096^3 call, alternating runs on one box
+    st_na_v4(o, v[0].x, v[1].x, v[2].x, v[3].x);
+    st_na_v4(o + 512, v[0].y, v[1].y, v[2].y, v[3].y);
+    st_na_v4(o + 1024, v[0].z, v[1].z, v[2].z, v[3].z);
+    st_na_v4(o + 1536, v[0].w, v[1].w, v[2].w, v[3].w);
 }
 
 int validate(const SfRelayoutDesc &d)
