@@ -225,11 +225,12 @@ int validate_call(const GroupDesc *groups, int num_groups)
 // re-reads and the TMA operations per output byte, which the measurements on
 // GB300 show matters for every shape here; they need every N to be a multiple
 // of 256 (a B tile takes two whole 128-row scale blocks).  Otherwise BN = 128
-// with 512-K stages (CfgStream).  CTA pairs (CfgPair, 256 x 256 tiles) run a
-// 256 x 256 tile in about 0.92 of the time one CTA takes for a 128 x 256
-// tile, but pad M to 256: they are chosen when the call fills at least four
-// rounds of the grid and pairing does not add a round (large M, e.g. the
-// 4096^3 groups), never for the small-M MoE shapes.  Stream-K (WIDE_SK) is
+// with 512-K stages (CfgStream).  A call that fits one round of the grid in
+// 128 x 128 tiles runs them (CfgCompute).  CTA pairs (CfgPair, 256 x 256
+// tiles) run a 256 x 256 tile in about 0.92 of the time one CTA takes for a
+// 128 x 256 tile, but pad M to 256: they are chosen when pairing does not
+// add a round of the grid (large M, e.g. the 4096^3 groups, and calls of
+// fewer tiles than SMs), never for the small-M MoE shapes.  Stream-K (WIDE_SK) is
 // never chosen here: on GB300 it measured slower than whole tiles even where
 // it removes the most idle time (fewer tiles than SMs: 2 groups of 512 x
 // 3072 x 4096, 33.7 vs 21.2 us): its ranges start at scattered K offsets, so
@@ -245,7 +246,7 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
                            ? kKindWide
                            : forced_env;
     bool all_n256 = true, all_n_ge256 = true;
-    long long wide_tiles = 0, pair_tiles = 0;
+    long long wide_tiles = 0, pair_tiles = 0, narrow_tiles = 0;
     for (int i = 0; i < n; ++i)
         if (groups[i].M > 0) {
             const GroupDesc &g = groups[i];
@@ -253,6 +254,7 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
             all_n_ge256 = all_n_ge256 && (g.N >= 256);
             wide_tiles += (long long)((g.M + 127) / 128) * ((g.N + 255) / 256);
             pair_tiles += (long long)((g.M + 255) / 256) * ((g.N + 255) / 256);
+            narrow_tiles += (long long)((g.M + 127) / 128) * ((g.N + 127) / 128);
         }
     if (forced >= 0 && forced < kNumKinds) {
         if (needs_n256(forced) && !all_n256)
@@ -275,7 +277,20 @@ int choose_kind(const GroupDesc *groups, int n, int sm_count, bool need_bn256 = 
     const int pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
     const long long rounds_wide = (wide_tiles + sm_count - 1) / (sm_count > 0 ? sm_count : 1);
     const long long rounds_pair = (pair_tiles + pairs - 1) / pairs;
-    if (all_n_ge256 && rounds_wide >= 4 && rounds_pair <= rounds_wide)
+    // A call whose 128 x 128 tiles fit one round of the grid runs them: twice
+    // the CTAs of 128 x 256 tiles, each with half the work (GEMM us, 128 x 128
+    // against 128 x 256: 4 x [256, 2048, 2048] 7.8 / 10.2, 8 x [128, 1024,
+    // 4096] 11.1 / 14.4, 6 x [300, 1024, 1024] 5.5 / 7.4, 2 x [M, 256, 256]
+    // 3.7 / 5.3).  SwiGLU needs the 256-column tile.
+    if (!need_bn256 && narrow_tiles <= sm_count)
+        return kKindCompute;
+    // CTA pairs whenever they need no more rounds of the grid than single
+    // CTAs: each SM then stages half the B bytes (4096^3 groups 14 / 14
+    // rounds; 2 x [512, 3072, 4096] 1 / 1, 14.0 against 14.3 us; 2 x [1000,
+    // 4096, 2048] 2 / 2, 14.6 against 15.5 us), but not when padding M to 256
+    // rows adds a round (the MoE shapes: gate/up 3 / 2, down 5 / 4; 8 x [64,
+    // 4096, 7168] 2 / 1, 33.8 against 26.8 us)
+    if (all_n_ge256 && rounds_pair <= rounds_wide)
         return kKindPair;
     return all_n256 ? kKindWide : kKindStream;
 }

@@ -105,15 +105,17 @@ int nvfp4_group_gemm_ex(const GroupDesc *groups, int num_groups, const GemmEpilo
 
 /* Kernel configurations of the grouped GEMM (chosen per call from the
  * shapes; the environment variable NVFP4_GEMM_KIND forces one):
- *  STREAM  128 x 128 tiles, 512-K stages (any N)
+ *  STREAM  128 x 128 tiles, 512-K stages (any N): larger calls with an N
+ *          that is not a multiple of 256
  *  WIDE    128 x 256 tiles, 256-K stages (every N a multiple of 256)
- *  COMPUTE 128 x 128 tiles, 256-K stages, 64-column stores
+ *  COMPUTE 128 x 128 tiles, 256-K stages, 64-column stores (any N): calls
+ *          whose 128 x 128 tiles fit one round of the grid
  *  WIDE512 128 x 256 tiles, 512-K stages
  *  WIDE_P2 / WIDE_P4  accepted for compatibility; the same as WIDE (every
  *          configuration spreads a stage's loads over four issuing warps)
  *  PAIR    256 x 256 tiles on CTA pairs (tcgen05 cta_group::2; N >= 256):
- *          chosen for large M, when pairing fills at least four rounds of
- *          the grid without adding one
+ *          chosen whenever pairing does not add a round of the grid (large
+ *          M; calls of fewer tiles than SMs)
  *  WIDE_SK WIDE tiles with stream-K: the call's (tile, 256-K stage) units
  *          are cut into one equal contiguous range per SM, so a tile may be
  *          split between CTAs; the CTA holding a tile's first stages adds

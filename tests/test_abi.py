@@ -147,27 +147,36 @@ def _plan(lib, shapes, sm=152):
 
 
 @pytest.mark.parametrize("shapes,sm,kind,launches", [
-    # small-M MoE shapes, every N a multiple of 256: 128 x 256 tiles
+    # small-M MoE shapes, every N a multiple of 256: 128 x 256 tiles (pairs
+    # would pad M to 256 rows and add a round of the grid)
     ([(m, 4096, 7168) for m in MOE_M], 152, "wide", 1),
     ([(m, 7168, 2048) for m in MOE_M], 152, "wide", 1),
+    ([(64, 4096, 7168)] * 8, 152, "wide", 1),
     # 2048 tiles of 128 x 256 = 14 rounds of 152; 1024 pair tiles = 14 rounds of 76
     ([(4096, 4096, 4096)] * 4, 152, "pair", 1),
-    # one round of tiles: no pairs ...
-    ([(512, 3072, 4096)] * 2, 152, "wide", 1),
-    # ... but 12 rounds on 8 SMs, and pairing adds none
+    # fewer tiles than SMs: pairs need no more rounds (1 = 1) ...
+    ([(512, 3072, 4096)] * 2, 152, "pair", 1),
+    ([(1000, 4096, 2048)] * 2, 152, "pair", 1),
+    # ... and the same on 8 SMs (12 = 12 rounds)
     ([(512, 3072, 4096)] * 2, 8, "pair", 1),
     # 768 tiles = 6 rounds, 512 pair tiles = 7 rounds of 76: pairing would add one
     ([(384, 4096, 256)] * 16, 152, "wide", 1),
-    ([(64, 256, 256), (128, 256, 256)], 152, "wide", 1),
-    # one N off the 256 grid sends the whole call to 128-column tiles
-    ([(77, 136, 512)], 152, "stream", 1),
+    # 128 x 128 tiles that fit one round of the grid
+    ([(64, 256, 256), (128, 256, 256)], 152, "compute", 1),
+    ([(256, 2048, 2048)] * 4, 152, "compute", 1),
+    ([(300, 1024, 1024)] * 6, 152, "compute", 1),
+    ([(77, 136, 512)], 152, "compute", 1),
+    # ... but not past it: 160 tiles of 128 x 128 on 152 SMs
+    ([(128, 256, 256)] * 80, 152, "wide", 3),
+    # one N off the 256 grid sends a larger call to 128-column tiles
     ([(4096, 4096, 4096), (64, 136, 256)], 152, "stream", 1),
+    ([(300, 264, 4096)] * 60, 152, "stream", 2),
     # 32 groups per launch; empty groups take no slot
-    ([(64, 256, 256)] * 32, 152, "wide", 1),
-    ([(64, 256, 256)] * 33, 152, "wide", 2),
-    ([(64, 256, 256)] * 65, 152, "wide", 3),
-    ([(0, 256, 256)] * 40 + [(64, 256, 256)] * 30, 152, "wide", 1),
-    ([(0, 256, 256)] * 3, 152, "wide", 0),
+    ([(64, 256, 256)] * 32, 152, "compute", 1),
+    ([(64, 256, 256)] * 33, 152, "compute", 2),
+    ([(64, 256, 256)] * 65, 152, "compute", 3),
+    ([(0, 256, 256)] * 40 + [(64, 256, 256)] * 30, 152, "compute", 1),
+    ([(0, 256, 256)] * 3, 152, "compute", 0),
 ])
 def test_plan_kind_and_launches(lib, monkeypatch, shapes, sm, kind, launches):
     monkeypatch.delenv("NVFP4_GEMM_KIND", raising=False)

@@ -256,9 +256,11 @@ def test_step_graph_replays_new_inputs(kind):
 
 
 def test_plan_picks_by_shape_class():
-    """The configuration the library picks per shape class: CTA pairs for
-    the 4096^3 groups, 128 x 256 tiles for the small-M MoE shapes, 128 x 128
-    tiles when some N is not a multiple of 256; one launch per 32 groups."""
+    """The configuration the library picks per shape class on this GPU: CTA
+    pairs for the 4096^3 groups and for calls of fewer tiles than SMs, 128 x
+    256 tiles for the small-M MoE shapes, 128 x 128 tiles for calls that fit
+    one round of the grid in them and when some N of a larger call is not a
+    multiple of 256; one launch per 32 groups."""
     from block_scaled_nvfp4_group_gb300 import ops, workloads
     from block_scaled_nvfp4_group_gb300.device import DeviceProblem
 
@@ -267,9 +269,13 @@ def test_plan_picks_by_shape_class():
 
     assert plan(workloads.make_workload("square").groups) == ("pair", 1)
     assert plan(workloads.make_workload("moe_gate_up").groups) == ("wide", 1)
-    assert plan(workloads.make_groups([(300, 264, 256)], seed=1)) == ("stream", 1)
+    assert plan(workloads.make_workload("moe_down").groups) == ("wide", 1)
+    assert plan(workloads.make_workload("quantized").groups) == ("pair", 1)
+    assert plan(workloads.make_workload("tiny").groups) == ("compute", 1)
+    assert plan(workloads.make_groups([(300, 264, 256)], seed=1)) == ("compute", 1)
+    assert plan(workloads.make_groups([(300, 264, 256)] * 60, seed=1)) == ("stream", 2)
     shapes = [(64, 256, 256)] * 40
-    assert plan(workloads.make_groups(shapes, seed=1)) == ("wide", 2)
+    assert plan(workloads.make_groups(shapes, seed=1)) == ("compute", 2)
 
 
 @pytest.mark.parametrize("shape", [(1, 1 << 20, 256), (1 << 20, 256, 256), (256, 256, 1 << 20)])
