@@ -183,6 +183,33 @@ def test_repeat_calls_identical():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("kind", [None, "pair", "stream"])
+def test_l2_hints_and_prefetch_leave_results_unchanged(kind, monkeypatch):
+    """The L2 eviction hint for B (normal / evict-first / evict-last) and the
+    optional L2 prefetch of B are performance settings only: every setting
+    gives bit-identical C, equal to the oracle's within the tolerance."""
+    from block_scaled_nvfp4_group_gb300 import workloads
+    from block_scaled_nvfp4_group_gb300.device import DeviceProblem
+    groups = workloads.make_groups([(64, 4096, 1024)] * 8 + [(190, 512, 2048)], seed=31)
+    ref = None
+    with gemm_env(kind):
+        run_and_compare(groups, rows_per_group=8, seed=3)
+        prob = DeviceProblem(groups)
+        for policy, pf in [("0", "0"), ("1", "0"), ("2", "0"), ("2", "3")]:
+            monkeypatch.setenv("NVFP4_B_POLICY", policy)
+            monkeypatch.setenv("NVFP4_PF_STAGES", pf)
+            for c in prob.C:
+                c.fill_(float("nan"))
+            prob.step()
+            torch.cuda.synchronize()
+            out = [c.clone().view(torch.int16) for c in prob.C]
+            if ref is None:
+                ref = out
+            else:
+                for a, b in zip(ref, out):
+                    assert torch.equal(a, b), (policy, pf)
+
+
 # --- the benchmark workloads, in the launch configuration bench.py times -----
 
 def test_workload_tiny():
