@@ -166,8 +166,13 @@ def _plan(lib, shapes, sm=152):
     ([(256, 2048, 2048)] * 4, 152, "compute", 1),
     ([(300, 1024, 1024)] * 6, 152, "compute", 1),
     ([(77, 136, 512)], 152, "compute", 1),
-    # ... but not past it: 160 tiles of 128 x 128 on 152 SMs
+    # ... up to exactly one round (152 tiles of 128 x 128) but not past it
+    # (154, 160): then 128 x 256 tiles, since pairs would need two rounds
+    ([(128, 256, 256)] * 76, 152, "compute", 3),
+    ([(128, 256, 256)] * 77, 152, "wide", 3),
     ([(128, 256, 256)] * 80, 152, "wide", 3),
+    # SM count of the plan: the same call on 8 SMs is many rounds of pairs
+    ([(256, 2048, 2048)] * 4, 8, "pair", 1),
     # one N off the 256 grid sends a larger call to 128-column tiles
     ([(4096, 4096, 4096), (64, 136, 256)], 152, "stream", 1),
     ([(300, 264, 4096)] * 60, 152, "stream", 2),
