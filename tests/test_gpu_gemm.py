@@ -224,7 +224,7 @@ def test_workload_quantized(kind):
         run_and_compare(workloads.make_workload("quantized").groups)
 
 
-@pytest.mark.parametrize("kind", [None, "swap", "stream", "wide512", "compute", "pair"])
+@pytest.mark.parametrize("kind", [None, "swap", "stream", "wide512", "compute", "pair", "wide_sk"])
 def test_workload_moe_down(kind):
     from block_scaled_nvfp4_group_gb300 import workloads
     with gemm_env(kind):
